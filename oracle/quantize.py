@@ -1,0 +1,84 @@
+"""Per-tensor and 32x32 block amax -> scale -> E4M3 quantisation.
+
+[P1] (risks paragraph) states that E4M3's range is +-448 and that per-tensor
+scaling is needed to avoid overflow ("需 per-tensor 缩放避免溢出"), and the
+parameter list fixes the threshold "scale_max=448".  [P3] (implementation
+paragraph) sets the scale granularity to 32x32 blocks ("缩放粒度为 32x32 块").
+
+The steps, in the order the method takes them:
+
+1. amax = max_i |x_i| over the tensor (or tile), NaN ignored, in fp32.
+   Max is exact, so the order of the reduction does not matter.
+2. qscale = fp32(448 / amax), the multiplier applied before the cast, and
+   scale  = fp32(amax / 448), the dequantisation factor the GEMM consumes.
+   Both are single IEEE fp32 divisions; neither is derived from the other.
+   If amax == 0 or qscale is not finite, qscale = scale = 1.
+3. q_i = E4M3_RNE_satfinite(fp32(x_i * qscale)): one fp32 multiply, then the
+   saturating round-to-nearest-even encode.
+"""
+
+import numpy as np
+
+from .e4m3 import encode, E4M3_MAX
+
+_F448 = np.float32(E4M3_MAX)
+
+
+def amax_fp32(x):
+    """max |x| over all elements, NaN ignored, as an fp32 scalar (0 if none)."""
+    x = np.asarray(x, dtype=np.float32)
+    a = np.abs(x).reshape(-1)
+    a = a[~np.isnan(a)]
+    if a.size == 0:
+        return np.float32(0.0)
+    return np.float32(a.max())
+
+
+def scales_from_amax(amax):
+    """(qscale, scale) as fp32 scalars, by the two IEEE fp32 divisions."""
+    amax = np.float32(amax)
+    with np.errstate(divide="ignore", over="ignore", invalid="ignore"):
+        qscale = np.float32(_F448 / amax)
+        scale = np.float32(amax / _F448)
+    if amax == 0 or not np.isfinite(qscale):
+        return np.float32(1.0), np.float32(1.0)
+    return qscale, scale
+
+
+def quantize_pertensor(x):
+    """Quantise an fp32 array with one per-tensor scale.
+
+    Returns (codes uint8 with x's shape, amax fp32, scale fp32).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    amax = amax_fp32(x)
+    qscale, scale = scales_from_amax(amax)
+    with np.errstate(over="ignore", invalid="ignore"):
+        y = (x * qscale).astype(np.float32)      # fp32 * fp32 -> fp32, RNE
+    return encode(y), amax, scale
+
+
+def quantize_blockwise_32x32(x):
+    """Quantise a 2-D fp32 array with one scale per 32x32 tile.
+
+    Tile (i, j) covers rows 32i..32i+31 and columns 32j..32j+31, cut short at
+    the array's edge (ragged edge tiles use their actual extent).  Each tile is
+    quantised exactly as ``quantize_pertensor`` quantises a whole tensor.
+
+    Returns (codes uint8 [R][C], scales fp32 [ceil(R/32)][ceil(C/32)]).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    if x.ndim != 2:
+        raise ValueError("expected a 2-D array")
+    R, C = x.shape
+    tr, tc = -(-R // 32), -(-C // 32)
+    codes = np.empty((R, C), dtype=np.uint8)
+    scales = np.empty((tr, tc), dtype=np.float32)
+    for i in range(tr):
+        for j in range(tc):
+            rs = slice(32 * i, min(32 * i + 32, R))
+            cs = slice(32 * j, min(32 * j + 32, C))
+            q, _, s = quantize_pertensor(x[rs, cs])
+            codes[rs, cs] = q
+            scales[i, j] = s
+    return codes, scales
