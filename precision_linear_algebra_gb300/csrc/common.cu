@@ -1,0 +1,131 @@
+// Library-wide state: the device status word, the wait limit, device
+// queries, the tensor-map encoder, status strings and the version.
+#include <atomic>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8la {
+
+// One status word per device (each device holds its own copy of this
+// module variable).  Kernels OR error bits into it.
+__device__ unsigned g_status_word = 0;
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned *g_status_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+int g_cc_major[kMaxDevices] = {};
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+EncodeTiledFn g_encode = nullptr;
+bool g_encode_tried = false;
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return -1;
+  return dev;
+}
+
+bool fill_device_info(int dev) {
+  if (g_sm_count[dev] > 0) return true;
+  int sms = 0, major = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) !=
+          cudaSuccess)
+    return false;
+  g_sm_count[dev] = sms;
+  g_cc_major[dev] = major;
+  return true;
+}
+}  // namespace
+
+unsigned *status_word_ptr() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_status_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<unsigned *>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+uint64_t wait_timeout_ns() { return g_timeout_ns.load(); }
+
+int sm_count() {
+  const int dev = current_device();
+  if (dev < 0) return -1;
+  std::lock_guard<std::mutex> lock(g_mu);
+  return fill_device_info(dev) ? g_sm_count[dev] : -1;
+}
+
+bool device_is_sm10x() {
+  const int dev = current_device();
+  if (dev < 0) return false;
+  std::lock_guard<std::mutex> lock(g_mu);
+  return fill_device_info(dev) && g_cc_major[dev] == 10;
+}
+
+EncodeTiledFn encode_tiled_fn() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_encode_tried) {
+    g_encode_tried = true;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  return g_encode;
+}
+
+}  // namespace fp8la
+
+extern "C" {
+
+fp8la_status fp8_get_device_status(fp8la_stream_t stream) {
+  unsigned *p = fp8la::status_word_ptr();
+  if (!p) return FP8LA_ERR_CUDA;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return FP8LA_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FP8LA_ERR_CUDA;
+  if (v != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) !=
+        cudaSuccess)
+      return FP8LA_ERR_CUDA;
+  }
+  return (v & fp8la::kStatusTimeout) ? FP8LA_ERR_DEVICE_TIMEOUT : FP8LA_OK;
+}
+
+fp8la_status fp8la_set_wait_timeout_ns(int64_t timeout_ns) {
+  if (timeout_ns < 1000) return FP8LA_ERR_INVALID_ARG;
+  fp8la::g_timeout_ns.store(static_cast<uint64_t>(timeout_ns));
+  return FP8LA_OK;
+}
+
+const char *fp8la_status_string(fp8la_status s) {
+  switch (s) {
+    case FP8LA_OK: return "FP8LA_OK";
+    case FP8LA_ERR_INVALID_ARG: return "FP8LA_ERR_INVALID_ARG";
+    case FP8LA_ERR_ALIGNMENT: return "FP8LA_ERR_ALIGNMENT";
+    case FP8LA_ERR_UNSUPPORTED: return "FP8LA_ERR_UNSUPPORTED";
+    case FP8LA_ERR_CUDA: return "FP8LA_ERR_CUDA";
+    case FP8LA_ERR_DEVICE_TIMEOUT: return "FP8LA_ERR_DEVICE_TIMEOUT";
+    default: return "FP8LA_ERR_UNKNOWN";
+  }
+}
+
+int fp8la_version(void) { return 100; }
+
+}  // extern "C"

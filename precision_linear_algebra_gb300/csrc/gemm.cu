@@ -1,0 +1,555 @@
+// Per-tensor-scaled and grouped (MoE) E4M3 GEMMs on tcgen05 tensor cores.
+//
+// Method: [P1] "通过 CUTLASS 命名约定在 Triton 中实现 FP8 GEMM 内核", kernel-code
+// paragraph (C tile = sum over K blocks of A tile x B tile, FP32
+// accumulator), scale paragraph (acc * scale_a * scale_b) and parameter
+// list (E4M3 in, FP32 accumulate, BF16 out); [P3] "JAX 中使用 Triton 优化
+// Blackwell GPU 的 FP8 GEMM 内核", TMA paragraph, warp-specialisation
+// paragraph (one warp loads by TMA, one issues the MMA) and MoE paragraph
+// (grouped GEMM over experts).
+//
+// Design (sm_103a, one CTA per SM, persistent):
+//   * warp 4 (one lane): TMA producer.  For every 128-wide K block it loads
+//     a 128 x 128 A tile and a BN x 128 B tile (both K-major, 128-byte
+//     swizzle) into one stage of a STAGES-deep shared-memory ring, arming
+//     the stage's `full` mbarrier with the byte count.
+//   * warp 5 (one lane): MMA issuer.  Four tcgen05.mma kind::f8f6f4
+//     (M=128, N=BN, K=32 each) per stage into an FP32 accumulator in tensor
+//     memory; tcgen05.commit frees the stage (`empty`) and, after the last
+//     K block, hands the accumulator to the epilogue (`tmem_full`).
+//     Tensor memory holds two accumulators (2 x BN of 512 columns) so the
+//     epilogue of tile i overlaps the MMAs of tile i+1.
+//   * warps 0-3: epilogue.  Warp w owns TMEM lanes (= C rows) 32w..32w+31;
+//     each thread loads its row's accumulator 32 columns at a time
+//     (tcgen05.ld), multiplies by scale_a*scale_b, rounds to BF16 and writes
+//     16-byte vectors; then releases the accumulator (`tmem_empty`).
+//   * Tiles are visited in a grouped order (GROUP_M row blocks per group)
+//     so that concurrently running CTAs share A and B tiles through L2.
+//   * Ragged M, N, K: TMA fills out-of-range operand elements with zeros;
+//     the epilogue stores only in-range elements.
+//   * Grouped GEMM: A is the concatenation of all groups' rows; B is a 3-D
+//     tensor [E][N][K].  The tile space is the concatenation of every
+//     group's own tile grid; each CTA derives it from m_offsets on the
+//     device.  Rows of a tile past its group's end are computed (they hold
+//     the next group's rows, or TMA zeros) and not stored.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8la {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 128;                  // bytes = E4M3 values per K block
+constexpr int UMMA_K = 32;               // K per tcgen05.mma for 8-bit inputs
+constexpr int kThreads = 192;            // 6 warps
+constexpr int kMaxGroups = 1024;
+constexpr int GROUP_M = 16;
+
+struct GemmArgs {
+  uint16_t *C;
+  int64_t ldc;
+  int32_t M, N, K;
+  const float *scale_a;  // per-tensor: [1]; grouped: [E]
+  const float *scale_b;
+  const int32_t *m_offsets;  // grouped only
+  int32_t num_groups;        // grouped only
+  unsigned *status;
+  uint64_t timeout_ns;
+  int32_t withhold_first;  // diagnostic: skip the first TMA arrival
+  int32_t c_vec16;         // C rows allow 16-byte stores (C 16-byte aligned, ldc % 8 == 0)
+};
+
+template <int BN, int STAGES>
+struct Smem {
+  static constexpr int kABytes = BM * BK;
+  static constexpr int kBBytes = BN * BK;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN;  // two accumulators
+  // Layout (offsets from a 1024-byte-aligned base).
+  static constexpr int kA = 0;
+  static constexpr int kB = kA + STAGES * kABytes;
+  static constexpr int kBar = kB + STAGES * kBBytes;
+  static constexpr int kNumBars = 2 * STAGES + 4 + 1;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kPrefix = kMisc + 16;  // int32 [kMaxGroups + 1]
+  static constexpr int kEnd = kPrefix + (kMaxGroups + 1) * 4;
+  static constexpr int kAlloc = kEnd + 1024;  // slack for aligning the base
+};
+
+// Tile t of a tiles_m x tiles_n grid in grouped order.
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n,
+                                            int &mb, int &nb) {
+  const int per_group = GROUP_M * tiles_n;
+  const int g = t / per_group;
+  const int first_m = g * GROUP_M;
+  const int gm = min(tiles_m - first_m, GROUP_M);
+  const int r = t - g * per_group;
+  mb = first_m + r % gm;
+  nb = r / gm;
+}
+
+struct TileInfo {
+  int32_t row0;     // first C row of the tile
+  int32_t row_end;  // rows >= row_end are not stored
+  int32_t n0;
+  int32_t group;
+};
+
+template <bool GROUPED>
+__device__ __forceinline__ TileInfo tile_info(int t, const GemmArgs &a,
+                                              int tiles_n, const int32_t *pref,
+                                              const int32_t *offs_smem,
+                                              int BN) {
+  TileInfo ti;
+  if (!GROUPED) {
+    const int tiles_m = (a.M + BM - 1) / BM;
+    int mb, nb;
+    tile_coords(t, tiles_m, tiles_n, mb, nb);
+    ti.row0 = mb * BM;
+    ti.row_end = a.M;
+    ti.n0 = nb * BN;
+    ti.group = 0;
+  } else {
+    // pref[e] = number of tiles of groups 0..e-1; find e with
+    // pref[e] <= t < pref[e+1] (binary search over num_groups + 1 entries).
+    int lo = 0, hi = a.num_groups;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (pref[mid] <= t) lo = mid; else hi = mid;
+    }
+    const int e = lo;
+    const int m_lo = offs_smem[e], m_hi = offs_smem[e + 1];
+    const int tiles_m = (m_hi - m_lo + BM - 1) / BM;
+    int mb, nb;
+    tile_coords(t - pref[e], tiles_m, tiles_n, mb, nb);
+    ti.row0 = m_lo + mb * BM;
+    ti.row_end = m_hi;
+    ti.n0 = nb * BN;
+    ti.group = e;
+  }
+  return ti;
+}
+
+template <int BN, int STAGES, bool GROUPED>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_e4m3_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB,
+                     const GemmArgs a) {
+  using L = Smem<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t *sbase = smem_raw + (base - raw_addr);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const uint32_t bar0 = base + L::kBar;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t final_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + L::kMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(sbase + L::kMisc + 4);
+  int32_t *pref = reinterpret_cast<int32_t *>(sbase + L::kPrefix);
+  __shared__ int32_t offs_smem[GROUPED ? kMaxGroups + 1 : 1];
+
+  const int tiles_n = (a.N + BN - 1) / BN;
+  const int nkb = (a.K + BK - 1) / BK;
+
+  // ---------------------------------------------------------------- setup
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), BM);  // every epilogue thread arrives
+    }
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_addr(tmem_slot), L::kTmemCols);
+    tmem_relinquish();
+  }
+  int total_tiles;
+  if (GROUPED) {
+    // Per-group tile counts and their exclusive prefix sum (warp 0).
+    if (warp == 0) {
+      for (int e = lane; e <= a.num_groups; e += 32) offs_smem[e] = a.m_offsets[e];
+      __syncwarp();
+      if (lane == 0) {
+        int acc = 0;
+        for (int e = 0; e < a.num_groups; ++e) {
+          pref[e] = acc;
+          const int me = offs_smem[e + 1] - offs_smem[e];
+          acc += (me > 0 ? (me + BM - 1) / BM : 0) * tiles_n;
+        }
+        pref[a.num_groups] = acc;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  total_tiles = GROUPED ? pref[a.num_groups]
+                        : ((a.M + BM - 1) / BM) * tiles_n;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t s = 0, ph = 0;
+      uint32_t issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        const TileInfo ti =
+            tile_info<GROUPED>(t, a, tiles_n, pref, offs_smem, BN);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns, a.status,
+                         abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = base + L::kA + s * L::kABytes;
+          const uint32_t sb = base + L::kB + s * L::kBBytes;
+          if (!(a.withhold_first && issued == 0)) {
+            mbar_arrive_expect_tx(full_bar(s), L::kStageBytes);
+            tma_load_2d(sa, &tmA, full_bar(s), kb * BK, ti.row0);
+            if (GROUPED)
+              tma_load_3d(sb, &tmB, full_bar(s), kb * BK, ti.n0, ti.group);
+            else
+              tma_load_2d(sb, &tmB, full_bar(s), kb * BK, ti.n0);
+          }
+          ++issued;
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+      }
+      // Drain: wait for the last load issued into each stage, so that no
+      // copy is still writing shared memory when the CTA exits.
+      for (uint32_t st = 0; st < STAGES; ++st) {
+        if (issued <= st) break;
+        const uint32_t arms = (issued - 1 - st) / STAGES + 1;
+        if (a.withhold_first && st == 0 && arms == 1) continue;
+        mbar_wait_drain(full_bar(st), (arms - 1) & 1u, a.timeout_ns, a.status);
+      }
+    }
+  } else if (warp == 5) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+      uint32_t s = 0, ph = 0;
+      uint32_t local = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total_tiles;
+           t += gridDim.x, ++local) {
+        const uint32_t buf = local & 1u, use = local >> 1;
+        if (!mbar_wait(tempty_bar(buf), (use & 1u) ^ 1u, a.timeout_ns,
+                       a.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * BN;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(full_bar(s), ph, a.timeout_ns, a.status,
+                         abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc =
+              smem_desc_k128_sw128(base + L::kA + s * L::kABytes);
+          const uint64_t bdesc =
+              smem_desc_k128_sw128(base + L::kB + s * L::kBBytes);
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            // +32 bytes along K inside the 128-byte swizzled row = +2 in
+            // the descriptor's (address >> 4) field.
+            umma_f8f6f4(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc,
+                        (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty_bar(s));
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(tfull_bar(buf));
+      }
+      // Make sure every MMA issued has finished before tensor memory is
+      // released at exit.
+      umma_commit(final_bar);
+      mbar_wait_drain(final_bar, 0, a.timeout_ns, a.status);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    uint32_t local = 0;
+    float scale = 1.0f;
+    int cur_group = -1;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++local) {
+      const TileInfo ti =
+          tile_info<GROUPED>(t, a, tiles_n, pref, offs_smem, BN);
+      if (ti.group != cur_group) {
+        scale = __fmul_rn(a.scale_a[ti.group], a.scale_b[ti.group]);
+        cur_group = ti.group;
+      }
+      const uint32_t buf = local & 1u, use = local >> 1;
+      // The whole warp must agree before the warp-collective tcgen05.ld.
+      const bool ready = mbar_wait(tfull_bar(buf), use & 1u, a.timeout_ns,
+                                   a.status, abort_flag);
+      if (!__all_sync(0xffffffffu, ready)) break;
+      tc_fence_after();
+      const int row = ti.row0 + warp * 32 + lane;
+      const bool row_ok = row < ti.row_end && row < ti.row0 + BM;
+      uint16_t *crow = a.C + static_cast<int64_t>(row) * a.ldc;
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + buf * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(taddr + c, v);
+        const int n = ti.n0 + c;
+        if (row_ok && n < a.N) {
+          uint32_t w[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(
+                __fmul_rn(__uint_as_float(v[2 * j]), scale),
+                __fmul_rn(__uint_as_float(v[2 * j + 1]), scale));
+            w[j] = *reinterpret_cast<const uint32_t *>(&h);
+          }
+          if (a.c_vec16 && n + 32 <= a.N) {
+            uint4 *dst = reinterpret_cast<uint4 *>(crow + n);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2],
+                                  w[4 * j + 3]);
+          } else {
+            for (int j = 0; j < 32 && n + j < a.N; ++j)
+              crow[n + j] = static_cast<uint16_t>(
+                  (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty_bar(buf));
+    }
+  }
+
+  // ------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, L::kTmemCols);
+  }
+}
+
+__global__ void zero_c_kernel(uint16_t *C, int64_t ldc, int64_t M, int64_t N) {
+  const int64_t n = M * N;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       i < n; i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / N, c = i - r * N;
+    C[r * ldc + c] = 0;
+  }
+}
+
+// Grouped variant of the K = 0 case: zero the rows each group owns.
+__global__ void zero_c_grouped_kernel(uint16_t *C, int64_t ldc,
+                                      const int32_t *m_offsets, int32_t E,
+                                      int64_t N) {
+  const int64_t rows = m_offsets[E];
+  const int64_t n = rows * N;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       i < n; i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / N, c = i - r * N;
+    C[r * ldc + c] = 0;
+  }
+}
+
+constexpr int kBN = 256;
+constexpr int kStages = 4;
+
+bool encode_2d(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims,
+             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_3d(CUtensorMap *m, const void *ptr, uint64_t d0, uint64_t d1,
+               uint64_t d2, uint64_t s1, uint64_t s2, uint32_t b0,
+               uint32_t b1) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1, s2};
+  const cuuint32_t box[3] = {b0, b1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims,
+             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool GROUPED>
+fp8la_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB,
+                         const GemmArgs &args, int64_t max_tiles,
+                         cudaStream_t s) {
+  using L = Smem<kBN, kStages>;
+  auto kern = gemm_e4m3_kernel<kBN, kStages, GROUPED>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           L::kAlloc) != cudaSuccess)
+    return FP8LA_ERR_CUDA;
+  const int sms = sm_count();
+  if (sms <= 0) return FP8LA_ERR_CUDA;
+  int64_t grid = max_tiles < sms ? max_tiles : sms;
+  if (grid < 1) grid = 1;
+  kern<<<static_cast<int>(grid), kThreads, L::kAlloc, s>>>(tmA, tmB, args);
+  return launch_status();
+}
+
+fp8la_status check_operands(const uint8_t *A, int64_t lda, const uint8_t *B,
+                            int64_t ldb, const uint16_t *C, int64_t ldc,
+                            int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0) return FP8LA_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return FP8LA_OK;
+  if (!C || ldc < N) return FP8LA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(C) & 1u) != 0) return FP8LA_ERR_ALIGNMENT;
+  if (K == 0) return FP8LA_OK;
+  if (!A || !B || lda < K || ldb < K) return FP8LA_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || lda % 16 != 0 || ldb % 16 != 0)
+    return FP8LA_ERR_ALIGNMENT;
+  if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) ||
+      K >= (int64_t(1) << 31) || lda >= (int64_t(1) << 39) ||
+      ldb >= (int64_t(1) << 39))
+    return FP8LA_ERR_UNSUPPORTED;
+  return FP8LA_OK;
+}
+
+fp8la_status gemm_pertensor_impl(const uint8_t *A, int64_t lda,
+                                 const uint8_t *B, int64_t ldb, uint16_t *C,
+                                 int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                 const float *scale_a, const float *scale_b,
+                                 cudaStream_t s, int withhold) {
+  fp8la_status st = check_operands(A, lda, B, ldb, C, ldc, M, N, K);
+  if (st != FP8LA_OK) return st;
+  if (M == 0 || N == 0) return FP8LA_OK;
+  if (K > 0 && (!scale_a || !scale_b)) return FP8LA_ERR_INVALID_ARG;
+  if (!device_is_sm10x()) return FP8LA_ERR_UNSUPPORTED;
+  if (K == 0) {
+    const int sms = sm_count();
+    zero_c_kernel<<<sms > 0 ? sms * 4 : 1, 256, 0, s>>>(C, ldc, M, N);
+    return launch_status();
+  }
+  CUtensorMap tmA, tmB;
+  if (!encode_2d(&tmA, A, K, M, lda, BK, BM) ||
+      !encode_2d(&tmB, B, K, N, ldb, BK, kBN))
+    return FP8LA_ERR_CUDA;
+  unsigned *status = status_word_ptr();
+  if (!status) return FP8LA_ERR_CUDA;
+  GemmArgs args{};
+  args.C = C;
+  args.ldc = ldc;
+  args.M = static_cast<int32_t>(M);
+  args.N = static_cast<int32_t>(N);
+  args.K = static_cast<int32_t>(K);
+  args.scale_a = scale_a;
+  args.scale_b = scale_b;
+  args.status = status;
+  args.timeout_ns = wait_timeout_ns();
+  args.withhold_first = withhold;
+  args.c_vec16 = aligned16(C) && ldc % 8 == 0;
+  const int64_t tiles = ((M + BM - 1) / BM) * ((N + kBN - 1) / kBN);
+  return launch_gemm<false>(tmA, tmB, args, tiles, s);
+}
+
+}  // namespace
+}  // namespace fp8la
+
+using namespace fp8la;
+
+extern "C" fp8la_status fp8_gemm(const uint8_t *A, int64_t lda,
+                                 const uint8_t *B, int64_t ldb, uint16_t *C,
+                                 int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                 const float *scale_a, const float *scale_b,
+                                 fp8la_stream_t stream) {
+  return gemm_pertensor_impl(A, lda, B, ldb, C, ldc, M, N, K, scale_a,
+                             scale_b, reinterpret_cast<cudaStream_t>(stream),
+                             0);
+}
+
+extern "C" fp8la_status fp8la_diag_gemm_withheld_arrival(
+    const uint8_t *A, int64_t lda, const uint8_t *B, int64_t ldb, uint16_t *C,
+    int64_t ldc, const float *scale_a, const float *scale_b,
+    fp8la_stream_t stream) {
+  return gemm_pertensor_impl(A, lda, B, ldb, C, ldc, BM, kBN, BK, scale_a,
+                             scale_b, reinterpret_cast<cudaStream_t>(stream),
+                             1);
+}
+
+extern "C" fp8la_status fp8_grouped_gemm(
+    int32_t num_groups, const int32_t *m_offsets, int64_t m_capacity,
+    const uint8_t *A, int64_t lda, const uint8_t *B, int64_t ldb,
+    int64_t b_group_stride, uint16_t *C, int64_t ldc, int64_t N, int64_t K,
+    const float *scale_a, const float *scale_b, fp8la_stream_t stream) {
+  if (num_groups < 1 || num_groups > kMaxGroups || !m_offsets ||
+      m_capacity < 0)
+    return FP8LA_ERR_INVALID_ARG;
+  fp8la_status st = check_operands(A, lda, B, ldb, C, ldc, m_capacity, N, K);
+  if (st != FP8LA_OK) return st;
+  if (m_capacity == 0 || N == 0) return FP8LA_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!device_is_sm10x()) return FP8LA_ERR_UNSUPPORTED;
+  if (K == 0) {
+    const int sms = sm_count();
+    zero_c_grouped_kernel<<<sms > 0 ? sms * 4 : 1, 256, 0, s>>>(
+        C, ldc, m_offsets, num_groups, N);
+    return launch_status();
+  }
+  if (!scale_a || !scale_b) return FP8LA_ERR_INVALID_ARG;
+  if (b_group_stride % 16 != 0 || b_group_stride < N * ldb)
+    return b_group_stride % 16 != 0 ? FP8LA_ERR_ALIGNMENT
+                                    : FP8LA_ERR_INVALID_ARG;
+  CUtensorMap tmA, tmB;
+  if (!encode_2d(&tmA, A, K, m_capacity, lda, BK, BM) ||
+      !encode_3d(&tmB, B, K, N, num_groups, ldb, b_group_stride, BK, kBN))
+    return FP8LA_ERR_CUDA;
+  unsigned *status = status_word_ptr();
+  if (!status) return FP8LA_ERR_CUDA;
+  GemmArgs args{};
+  args.C = C;
+  args.ldc = ldc;
+  args.M = static_cast<int32_t>(m_capacity);
+  args.N = static_cast<int32_t>(N);
+  args.K = static_cast<int32_t>(K);
+  args.scale_a = scale_a;
+  args.scale_b = scale_b;
+  args.m_offsets = m_offsets;
+  args.num_groups = num_groups;
+  args.c_vec16 = aligned16(C) && ldc % 8 == 0;
+  args.status = status;
+  args.timeout_ns = wait_timeout_ns();
+  // Upper bound on the tile count without reading m_offsets: each group
+  // adds at most one partial row block.
+  const int64_t tiles =
+      ((m_capacity + BM - 1) / BM + num_groups) * ((N + kBN - 1) / kBN);
+  return launch_gemm<true>(tmA, tmB, args, tiles, s);
+}

@@ -1,0 +1,326 @@
+// E4M3 quantisers: per-tensor (amax grid reduction + cast) and 32x32 block.
+//
+// Method: [P1] "通过 CUTLASS 命名约定在 Triton 中实现 FP8 GEMM 内核", risks
+// paragraph (E4M3 spans +-448; per-tensor scaling avoids overflow) and
+// optimisation parameter list (scale_max = 448); [P3] "JAX 中使用 Triton 优化
+// Blackwell GPU 的 FP8 GEMM 内核", implementation paragraph (32x32 scale
+// blocks).  Per tensor (or tile): amax = max|x| (NaN ignored), qscale =
+// fp32(448/amax), scale = fp32(amax/448) (amax == 0 or qscale not finite:
+// both 1), q = E4M3 round-to-nearest-even saturating of fp32(x * qscale).
+//
+// Both kernels are HBM-bound streams.  The per-tensor path is two launches:
+// a 128-bit-load grid reduction whose blocks combine their maxima with one
+// atomicMax on the float's bit pattern (non-negative floats order like
+// their unsigned bit patterns; max is exact, so the result does not depend
+// on the order), then a cast pass.  The block quantiser needs one pass: a
+// 32x32 fp32 tile (4 KB) fits one warp's registers.
+#include <cuda_fp8.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8la {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kBlocksPerSm = 4;
+constexpr float kE4M3Max = 448.0f;
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// fmaxf returns the non-NaN operand, so NaNs drop out of the maximum.
+__device__ __forceinline__ float max_abs4(float m, float4 v) {
+  return fmaxf(fmaxf(fmaxf(m, fabsf(v.x)), fmaxf(fabsf(v.y), fabsf(v.z))),
+               fabsf(v.w));
+}
+
+__device__ __forceinline__ void block_max_into(float v, float *out) {
+  __shared__ float red[kThreads / 32];
+  v = warp_max(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    v = (l < static_cast<int>(blockDim.x >> 5)) ? red[l] : 0.0f;
+    v = warp_max(v);
+    if (l == 0)
+      atomicMax(reinterpret_cast<unsigned *>(out), __float_as_uint(v));
+  }
+}
+
+struct Scales {
+  float qscale, scale;
+};
+
+__device__ __forceinline__ Scales scales_from_amax(float amax) {
+  Scales s;
+  s.qscale = __fdiv_rn(kE4M3Max, amax);
+  s.scale = __fdiv_rn(amax, kE4M3Max);
+  if (amax == 0.0f || !isfinite(s.qscale)) {
+    s.qscale = 1.0f;
+    s.scale = 1.0f;
+  }
+  return s;
+}
+
+// Two fp32 values -> two E4M3 codes (low byte = first value).
+__device__ __forceinline__ uint32_t cvt2(float a, float b, float qs) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
+      make_float2(__fmul_rn(a, qs), __fmul_rn(b, qs)), __NV_SATFINITE,
+      __NV_E4M3));
+}
+
+__device__ __forceinline__ uint32_t cvt4(float4 v, float qs) {
+  return cvt2(v.x, v.y, qs) | (cvt2(v.z, v.w, qs) << 16);
+}
+
+__device__ __forceinline__ uint8_t cvt1(float a, float qs) {
+  return static_cast<uint8_t>(
+      __nv_cvt_float_to_fp8(__fmul_rn(a, qs), __NV_SATFINITE, __NV_E4M3));
+}
+
+__device__ __forceinline__ float4 ld_stream4(const float4 *p) {
+  float4 v;
+  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// ------------------------------------------------------------------- amax
+// VEC = 4: x, ldx and cols allow 16-byte loads; VEC = 1: scalar loads.
+// A unit is VEC consecutive elements of one row; units are numbered row by
+// row, `upr` units per row.
+template <int VEC>
+__global__ void __launch_bounds__(kThreads)
+    amax_kernel(const float *__restrict__ x, int64_t rows, int64_t upr,
+                int64_t ldx, bool contiguous, float *amax_out) {
+  const int64_t n = rows * upr;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  float m = 0.0f;
+  if (VEC == 4) {
+    if (contiguous) {
+      const float4 *x4 = reinterpret_cast<const float4 *>(x);
+      for (; i + 3 * stride < n; i += 4 * stride) {
+        const float4 a = ld_stream4(x4 + i);
+        const float4 b = ld_stream4(x4 + i + stride);
+        const float4 c = ld_stream4(x4 + i + 2 * stride);
+        const float4 d = ld_stream4(x4 + i + 3 * stride);
+        m = max_abs4(max_abs4(m, a), b);
+        m = max_abs4(max_abs4(m, c), d);
+      }
+      for (; i < n; i += stride) m = max_abs4(m, ld_stream4(x4 + i));
+    } else {
+      for (; i < n; i += stride) {
+        const int64_t r = i / upr, c = i - r * upr;
+        m = max_abs4(m, ld_stream4(reinterpret_cast<const float4 *>(
+                            x + r * ldx + c * 4)));
+      }
+    }
+  } else {
+    for (; i < n; i += stride) {
+      const int64_t r = i / upr, c = i - r * upr;
+      m = fmaxf(m, fabsf(x[r * ldx + c]));
+    }
+  }
+  block_max_into(m, amax_out);
+}
+
+// ------------------------------------------------------------------- cast
+template <int VEC>
+__global__ void __launch_bounds__(kThreads)
+    cast_kernel(const float *__restrict__ x, int64_t rows, int64_t upr,
+                int64_t ldx, uint8_t *__restrict__ q, int64_t ldq,
+                bool contiguous, const float *amax_in, float *scale_out) {
+  const Scales s = scales_from_amax(*amax_in);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *scale_out = s.scale;
+  const float qs = s.qscale;
+  const int64_t n = rows * upr;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (VEC == 4) {
+    if (contiguous) {
+      const float4 *x4 = reinterpret_cast<const float4 *>(x);
+      uint32_t *q4 = reinterpret_cast<uint32_t *>(q);
+      for (; i + 3 * stride < n; i += 4 * stride) {
+        const float4 a = ld_stream4(x4 + i);
+        const float4 b = ld_stream4(x4 + i + stride);
+        const float4 c = ld_stream4(x4 + i + 2 * stride);
+        const float4 d = ld_stream4(x4 + i + 3 * stride);
+        q4[i] = cvt4(a, qs);
+        q4[i + stride] = cvt4(b, qs);
+        q4[i + 2 * stride] = cvt4(c, qs);
+        q4[i + 3 * stride] = cvt4(d, qs);
+      }
+      for (; i < n; i += stride) q4[i] = cvt4(ld_stream4(x4 + i), qs);
+    } else {
+      for (; i < n; i += stride) {
+        const int64_t r = i / upr, c = i - r * upr;
+        const float4 v = ld_stream4(
+            reinterpret_cast<const float4 *>(x + r * ldx + c * 4));
+        *reinterpret_cast<uint32_t *>(q + r * ldq + c * 4) = cvt4(v, qs);
+      }
+    }
+  } else {
+    for (; i < n; i += stride) {
+      const int64_t r = i / upr, c = i - r * upr;
+      q[r * ldq + c] = cvt1(x[r * ldx + c], qs);
+    }
+  }
+}
+
+// --------------------------------------------------------- 32x32 block cast
+// One warp per 32x32 tile.  VEC = 4: lane l covers columns 4*(l%8)..+3 of
+// rows l/8, l/8+4, ..., l/8+28 with 16-byte loads; VEC = 1: lane l covers
+// column l of all 32 rows.  Out-of-range elements are left out of the amax
+// and not stored.
+template <int VEC>
+__global__ void __launch_bounds__(256)
+    block32_kernel(const float *__restrict__ x, int64_t rows, int64_t cols,
+                   int64_t ldx, uint8_t *__restrict__ q, int64_t ldq,
+                   float *__restrict__ scales, int64_t ld_scales,
+                   int64_t tiles_r, int64_t tiles_c) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps_total =
+      static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) +
+                   (threadIdx.x >> 5);
+       t < tiles_r * tiles_c; t += warps_total) {
+    const int64_t tr = t / tiles_c, tc = t - tr * tiles_c;
+    const int64_t r0 = tr * 32, c0 = tc * 32;
+    if (VEC == 4) {
+      const int64_t col = c0 + 4 * (lane & 7);
+      const bool col_ok = col < cols;
+      float4 v[8];
+      float m = 0.0f;
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int64_t row = r0 + (lane >> 3) + 4 * it;
+        if (col_ok && row < rows) {
+          v[it] = ld_stream4(
+              reinterpret_cast<const float4 *>(x + row * ldx + col));
+          m = max_abs4(m, v[it]);
+        } else {
+          v[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      const float amax = warp_max(m);
+      const Scales s = scales_from_amax(amax);
+      if (lane == 0) scales[tr * ld_scales + tc] = s.scale;
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int64_t row = r0 + (lane >> 3) + 4 * it;
+        if (col_ok && row < rows)
+          *reinterpret_cast<uint32_t *>(q + row * ldq + col) =
+              cvt4(v[it], s.qscale);
+      }
+    } else {
+      const int64_t col = c0 + lane;
+      const bool col_ok = col < cols;
+      float v[32];
+      float m = 0.0f;
+#pragma unroll
+      for (int it = 0; it < 32; ++it) {
+        const int64_t row = r0 + it;
+        v[it] = (col_ok && row < rows) ? x[row * ldx + col] : 0.0f;
+        m = fmaxf(m, fabsf(v[it]));
+      }
+      const float amax = warp_max(m);
+      const Scales s = scales_from_amax(amax);
+      if (lane == 0) scales[tr * ld_scales + tc] = s.scale;
+#pragma unroll
+      for (int it = 0; it < 32; ++it) {
+        const int64_t row = r0 + it;
+        if (col_ok && row < rows) q[row * ldq + col] = cvt1(v[it], s.qscale);
+      }
+    }
+  }
+}
+
+int grid_for(int64_t units, int threads) {
+  const int sms = sm_count();
+  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * kBlocksPerSm;
+  int64_t g = (units + threads - 1) / threads;
+  if (g > cap) g = cap;
+  if (g < 1) g = 1;
+  return static_cast<int>(g);
+}
+
+}  // namespace
+}  // namespace fp8la
+
+using namespace fp8la;
+
+extern "C" fp8la_status fp8_quantize_pertensor(const float *x, int64_t rows,
+                                               int64_t cols, int64_t ldx,
+                                               uint8_t *q, int64_t ldq,
+                                               float *amax_out,
+                                               float *scale_out,
+                                               fp8la_stream_t stream) {
+  if (!amax_out || !scale_out || rows < 0 || cols < 0)
+    return FP8LA_ERR_INVALID_ARG;
+  const bool empty = rows == 0 || cols == 0;
+  if (!empty && (!x || !q || ldx < cols || ldq < cols))
+    return FP8LA_ERR_INVALID_ARG;
+  if (rows > (int64_t(1) << 40) || cols > (int64_t(1) << 40))
+    return FP8LA_ERR_UNSUPPORTED;
+  if (sm_count() <= 0) return FP8LA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(amax_out, 0, sizeof(float), s) != cudaSuccess)
+    return FP8LA_ERR_CUDA;
+  if (empty) {
+    cast_kernel<1><<<1, 32, 0, s>>>(x, 0, 0, 0, q, 0, true, amax_out,
+                                    scale_out);
+    return launch_status();
+  }
+  const bool vec4 = cols % 4 == 0 && ldx % 4 == 0 && ldq % 4 == 0 &&
+                    aligned16(x) &&
+                    (reinterpret_cast<uintptr_t>(q) & 3u) == 0;
+  const bool contiguous = ldx == cols && ldq == cols;
+  if (vec4) {
+    const int64_t upr = cols / 4;
+    const int g = grid_for(rows * upr, kThreads);
+    amax_kernel<4><<<g, kThreads, 0, s>>>(x, rows, upr, ldx, contiguous,
+                                          amax_out);
+    cast_kernel<4><<<g, kThreads, 0, s>>>(x, rows, upr, ldx, q, ldq,
+                                          contiguous, amax_out, scale_out);
+  } else {
+    const int g = grid_for(rows * cols, kThreads);
+    amax_kernel<1><<<g, kThreads, 0, s>>>(x, rows, cols, ldx, contiguous,
+                                          amax_out);
+    cast_kernel<1><<<g, kThreads, 0, s>>>(x, rows, cols, ldx, q, ldq,
+                                          contiguous, amax_out, scale_out);
+  }
+  return launch_status();
+}
+
+extern "C" fp8la_status fp8_quantize_blockwise_32x32(
+    const float *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q,
+    int64_t ldq, float *scales, int64_t ld_scales, fp8la_stream_t stream) {
+  if (rows < 0 || cols < 0) return FP8LA_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return FP8LA_OK;
+  const int64_t tiles_r = (rows + 31) / 32, tiles_c = (cols + 31) / 32;
+  if (!x || !q || !scales || ldx < cols || ldq < cols || ld_scales < tiles_c)
+    return FP8LA_ERR_INVALID_ARG;
+  if (rows > (int64_t(1) << 40) || cols > (int64_t(1) << 40))
+    return FP8LA_ERR_UNSUPPORTED;
+  if (sm_count() <= 0) return FP8LA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool vec4 = cols % 4 == 0 && ldx % 4 == 0 && ldq % 4 == 0 &&
+                    aligned16(x) &&
+                    (reinterpret_cast<uintptr_t>(q) & 3u) == 0;
+  const int g = grid_for(tiles_r * tiles_c * 32, 256);
+  if (vec4)
+    block32_kernel<4><<<g, 256, 0, s>>>(x, rows, cols, ldx, q, ldq, scales,
+                                        ld_scales, tiles_r, tiles_c);
+  else
+    block32_kernel<1><<<g, 256, 0, s>>>(x, rows, cols, ldx, q, ldq, scales,
+                                        ld_scales, tiles_r, tiles_c);
+  return launch_status();
+}

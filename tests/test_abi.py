@@ -1,0 +1,78 @@
+"""CPU checks of the C ABI: the library builds, loads, exports every entry
+point that include/*.h declares, and rejects bad arguments on the host
+before touching the GPU.  No compute call is made here."""
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"^\s*FP8LA_API\s+(?:const\s+)?\w+\s*\*?\s*(fp8\w*)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from precision_linear_algebra_gb300 import build
+    import precision_linear_algebra_gb300 as fl
+    build.build()
+    return fl.load()
+
+
+def test_header_declares_the_four_method_calls():
+    names = _declared()
+    for n in ["fp8_quantize_pertensor", "fp8_gemm", "fp8_gemm_blockscaled_32x32",
+              "fp8_grouped_gemm"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    import precision_linear_algebra_gb300 as fl
+    bound = {n for n, _, _ in fl.SIGNATURES}
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert name in bound, "binding lacks " + name
+
+
+def test_status_strings_and_version(lib):
+    assert lib.fp8la_status_string(0) == b"FP8LA_OK"
+    assert lib.fp8la_status_string(-5) == b"FP8LA_ERR_DEVICE_TIMEOUT"
+    assert lib.fp8la_version() >= 100
+
+
+def test_host_argument_rejection(lib):
+    """Validation that runs before any CUDA call."""
+    P = ctypes.c_void_p
+    one = P(16)
+    # quantize: NULL amax/scale, negative sizes, ld < cols
+    assert lib.fp8_quantize_pertensor(one, 4, 4, 4, one, 4, None, one, None) == -1
+    assert lib.fp8_quantize_pertensor(one, -1, 4, 4, one, 4, one, one, None) == -1
+    assert lib.fp8_quantize_pertensor(one, 4, 8, 4, one, 8, one, one, None) == -1
+    assert lib.fp8_quantize_blockwise_32x32(one, 4, 64, 64, one, 64, one, 1, None) == -1
+    # gemm: negative sizes, ldc < N, lda < K, misaligned operands
+    assert lib.fp8_gemm(one, 16, one, 16, one, 8, -1, 8, 16, one, one, None) == -1
+    assert lib.fp8_gemm(one, 16, one, 16, one, 4, 8, 8, 16, one, one, None) == -1
+    assert lib.fp8_gemm(one, 16, one, 32, one, 8, 8, 8, 32, one, one, None) == -1
+    assert lib.fp8_gemm(P(17), 32, one, 32, one, 8, 8, 8, 32, one, one, None) == -2
+    assert lib.fp8_gemm(one, 24, one, 32, one, 8, 8, 8, 24, one, one, None) == -2
+    assert lib.fp8_gemm(one, 16, one, 16, P(33), 8, 8, 8, 16, one, one, None) == -2
+    # M == 0 or N == 0 is a no-op that succeeds without touching the GPU
+    assert lib.fp8_gemm(None, 16, None, 16, None, 8, 0, 8, 16, None, None, None) == 0
+    assert lib.fp8_gemm(None, 16, None, 16, None, 8, 8, 0, 16, None, None, None) == 0
+    # grouped: group count out of range, NULL offsets
+    assert lib.fp8_grouped_gemm(0, one, 8, one, 16, one, 16, 256, one, 8, 8, 16, one, one, None) == -1
+    assert lib.fp8_grouped_gemm(2000, one, 8, one, 16, one, 16, 256, one, 8, 8, 16, one, one, None) == -1
+    assert lib.fp8_grouped_gemm(2, None, 8, one, 16, one, 16, 256, one, 8, 8, 16, one, one, None) == -1
+    # timeout setter
+    assert lib.fp8la_set_wait_timeout_ns(10) == -1
+    assert lib.fp8la_set_wait_timeout_ns(2_000_000_000) == 0

@@ -1,0 +1,142 @@
+"""GPU parity: per-tensor-scaled E4M3 GEMM against the oracle, within the bound
+
+    |C_gpu - C_ref| <= 2^-8 |C_ref| + 2^-22 K sa sb max|a| max|b|
+
+elementwise, C_ref being the oracle's exact product before its BF16 rounding
+(see the oracle's bound_pertensor)."""
+
+import numpy as np
+import pytest
+
+import oracle
+from _helpers import bf16_to_f64, check_pertensor, lib, random_codes, to_dev
+from precision_linear_algebra_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def _gemm(fl, A, B, sa, sb, ldc_pad=0):
+    import torch
+    M, K = A.shape
+    N = B.shape[0]
+    # TMA wants 16-byte row strides: pad K up to a multiple of 16
+    kp = max(16, (K + 15) // 16 * 16)
+    dA = torch.zeros((M, kp), dtype=torch.uint8, device="cuda")
+    dB = torch.zeros((N, kp), dtype=torch.uint8, device="cuda")
+    dA[:, :K] = to_dev(A)
+    dB[:, :K] = to_dev(B)
+    dA, dB = dA[:, :K], dB[:, :K]
+    dsa = torch.tensor([sa], dtype=torch.float32, device="cuda")
+    dsb = torch.tensor([sb], dtype=torch.float32, device="cuda")
+    Cs = torch.full((M, N + ldc_pad), -7.0, dtype=torch.bfloat16, device="cuda")
+    C = Cs[:, :N]
+    fl.gemm(dA, dB, dsa, dsb, C=C)
+    torch.cuda.synchronize()
+    assert fl.device_status() == 0
+    if ldc_pad:
+        assert torch.all(Cs[:, N:] == -7.0), "write past N"
+    return bf16_to_f64(C.contiguous())
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (128, 256, 128),    # one tile, one K block
+    (128, 256, 32),     # K shorter than one K block
+    (128, 256, 48),
+    (128, 256, 16),
+    (256, 512, 512),    # several tiles and K blocks
+    (128, 256, 1024),   # K blocks beyond the pipeline depth
+    (300, 270, 200),    # ragged M, N, K
+    (1, 1, 16),
+    (17, 8, 16),
+    (129, 257, 144),
+    (640, 1280, 384),
+])
+def test_random_codes(M, N, K):
+    fl = lib()
+    rng = np.random.default_rng(M * 7 + N * 13 + K)
+    A, B = random_codes(rng, (M, K)), random_codes(rng, (N, K))
+    sa, sb = np.float32(0.37), np.float32(1.9)
+    got = _gemm(fl, A, B, sa, sb)
+    frac = check_pertensor(got, A, B, sa, sb, what="%dx%dx%d" % (M, N, K))
+    assert frac > 0.99
+
+
+def test_identity_operand_selects_columns():
+    """A = I (code 0x38 = 1): C = dec(B)^T exactly (every E4M3 value is a bf16)."""
+    fl = lib()
+    rng = np.random.default_rng(3)
+    K = 128
+    A = np.where(np.eye(K, dtype=bool), 0x38, 0).astype(np.uint8)
+    B = random_codes(rng, (256, K))
+    got = _gemm(fl, A, B, np.float32(1), np.float32(1))
+    assert np.array_equal(got, oracle.decode(B).T)
+
+
+def test_one_hot_rows_and_ldc_padding():
+    fl = lib()
+    rng = np.random.default_rng(4)
+    M, N, K = 200, 300, 256
+    A = np.zeros((M, K), np.uint8)
+    A[np.arange(M), rng.integers(0, K, M)] = 0x40            # 2.0 at one k per row
+    B = random_codes(rng, (N, K))
+    got = _gemm(fl, A, B, np.float32(0.5), np.float32(1), ldc_pad=12)
+    check_pertensor(got, A, B, np.float32(0.5), np.float32(1), what="one-hot")
+
+
+def test_k_zero_writes_zeros():
+    fl = lib()
+    A = np.zeros((5, 0), np.uint8)
+    B = np.zeros((9, 0), np.uint8)
+    got = _gemm(fl, A, B, np.float32(1), np.float32(1))
+    assert got.shape == (5, 9) and np.all(got == 0)
+
+
+def test_saturated_operands():
+    fl = lib()
+    M, N, K = 128, 256, 512
+    A = np.full((M, K), 0x7E, np.uint8)
+    B = np.full((N, K), 0xFE, np.uint8)
+    got = _gemm(fl, A, B, np.float32(1), np.float32(1))
+    assert np.all(got == -448.0 * 448.0 * K)
+
+
+@pytest.mark.parametrize("n", [256, 1024])
+def test_square_configs_end_to_end(n):
+    """Quantise N(0,1) operands on the GPU, then GEMM; check both steps."""
+    import torch
+    fl = lib()
+    A, B = workloads.square(n, seed=0)
+    qa, _, sa = fl.quantize_pertensor(to_dev(A))
+    qb, _, sb = fl.quantize_pertensor(to_dev(B))
+    C = fl.gemm(qa, qb, sa, sb)
+    torch.cuda.synchronize()
+    rqa, _, rsa = oracle.quantize_pertensor(A)
+    rqb, _, rsb = oracle.quantize_pertensor(B)
+    assert np.array_equal(qa.cpu().numpy(), rqa) and np.array_equal(qb.cpu().numpy(), rqb)
+    assert sa.item() == rsa and sb.item() == rsb
+    frac = check_pertensor(bf16_to_f64(C), rqa, rqb, rsa, rsb, what="square %d" % n)
+    assert frac > 0.99
+
+
+def test_8192_outliers_sampled():
+    """Full-size 8192^3 with outliers, in the launch configuration the
+    benchmark times; the oracle checks 96 sampled rows x all columns plus
+    all rows x 64 sampled columns."""
+    import torch
+    fl = lib()
+    A, B = workloads.square_outliers(8192, seed=0)
+    qa, _, sa = fl.quantize_pertensor(to_dev(A))
+    qb, _, sb = fl.quantize_pertensor(to_dev(B))
+    C = fl.gemm(qa, qb, sa, sb)
+    torch.cuda.synchronize()
+    assert fl.device_status() == 0
+    qa_n, qb_n = qa.cpu().numpy(), qb.cpu().numpy()
+    rqa, _, rsa = oracle.quantize_pertensor(A)
+    rqb, _, rsb = oracle.quantize_pertensor(B)
+    assert np.array_equal(qa_n, rqa) and np.array_equal(qb_n, rqb)
+    Cn = bf16_to_f64(C)
+    rng = np.random.default_rng(8)
+    rows = np.sort(rng.choice(8192, 96, replace=False))
+    cols = np.sort(rng.choice(8192, 64, replace=False))
+    check_pertensor(Cn[rows], rqa, rqb, rsa, rsb, rows=rows, what="rows")
+    check_pertensor(Cn[:, cols], rqa, rqb, rsa, rsb, cols=cols, what="cols")

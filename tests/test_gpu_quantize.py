@@ -1,0 +1,151 @@
+"""GPU parity: quantisers against the oracle, bit for bit (codes and scales)."""
+
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from _helpers import lib, to_dev
+from precision_linear_algebra_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_pertensor(fl, x_np, ldx_pad=0, ldq_pad=0):
+    import torch
+    rows, cols = x_np.shape
+    xs = torch.empty((rows, cols + ldx_pad), dtype=torch.float32, device="cuda")
+    xs[:, :cols] = to_dev(x_np)
+    qs = torch.full((rows, cols + ldq_pad), 0xA5, dtype=torch.uint8, device="cuda")
+    x = xs[:, :cols]
+    q = qs[:, :cols]
+    q_out, amax, scale = fl.quantize_pertensor(x, q=q)
+    torch.cuda.synchronize()
+    assert fl.device_status() == 0
+    if ldq_pad:
+        assert torch.all(qs[:, cols:] == 0xA5), "write outside the row"
+    return q.cpu().numpy(), amax.item(), scale.item()
+
+
+def _assert_same(got, x_np):
+    q, amax, scale = got
+    rq, ramax, rscale = oracle.quantize_pertensor(x_np)
+    assert np.float32(amax).tobytes() == np.float32(ramax).tobytes()
+    assert np.float32(scale).tobytes() == np.float32(rscale).tobytes()
+    diff = np.flatnonzero(q.reshape(-1) != rq.reshape(-1))
+    assert diff.size == 0, "codes differ at %d places, first %d: got %#x want %#x (x=%r)" % (
+        diff.size, diff[0], q.reshape(-1)[diff[0]], rq.reshape(-1)[diff[0]], x_np.reshape(-1)[diff[0]])
+
+
+@pytest.mark.parametrize("n", [256, 1024])
+def test_pertensor_square_configs(n):
+    fl = lib()
+    A, B = workloads.square(n, seed=0)
+    for x in (A, B):
+        _assert_same(_run_pertensor(fl, x), x)
+
+
+@pytest.mark.parametrize("shape,ldx_pad,ldq_pad", [
+    ((1, 1), 0, 0), ((1, 3), 0, 0), ((7, 13), 0, 0), ((33, 64), 0, 0),
+    ((65, 100), 4, 16), ((3, 17), 3, 5), ((1000, 1001), 0, 0), ((5, 4096), 0, 0)])
+def test_pertensor_ragged_and_strided(shape, ldx_pad, ldq_pad):
+    fl = lib()
+    rng = np.random.default_rng(hash(shape) & 0xFFFF)
+    x = (rng.standard_normal(shape) * 3).astype(np.float32)
+    _assert_same(_run_pertensor(fl, x, ldx_pad, ldq_pad), x)
+
+
+def test_pertensor_special_values():
+    fl = lib()
+    x = np.array([[0.0, -0.0, np.nan, 1e-30, -1e-30, 3.0, -7.0, 2.0 ** -130, 448.0, -5.5]],
+                 dtype=np.float32)
+    _assert_same(_run_pertensor(fl, x), x)
+    z = np.zeros((4, 8), dtype=np.float32)
+    _assert_same(_run_pertensor(fl, z), z)
+    tiny = np.array([[1e-39, -5e-40, 0.0, 3e-45]], dtype=np.float32)
+    _assert_same(_run_pertensor(fl, tiny), tiny)
+    inf = np.array([[np.inf, 2.0, -3.0, np.nan]], dtype=np.float32)
+    _assert_same(_run_pertensor(fl, inf), inf)
+
+
+def test_pertensor_empty_writes_unit_scale():
+    import torch
+    fl = lib()
+    x = torch.empty((0, 16), dtype=torch.float32, device="cuda")
+    q, amax, scale = fl.quantize_pertensor(x)
+    torch.cuda.synchronize()
+    assert amax.item() == 0.0 and scale.item() == 1.0
+
+
+def test_pertensor_8192_outliers_full_size():
+    """The 8192^2 operands with 0.1% +-50 sigma outliers, bit for bit."""
+    fl = lib()
+    A, B = workloads.square_outliers(8192, seed=0)
+    for x in (A, B):
+        _assert_same(_run_pertensor(fl, x), x)
+
+
+def _sweep_chunk(fl, bits):
+    """Quantise one chunk of fp32 bit patterns with 448 appended (so that
+    chunks whose patterns stay within +-448 run with qscale == 1 and test the
+    cast alone) and compare with the oracle."""
+    x = np.concatenate([bits.view(np.float32), np.array([448.0], np.float32)])[None, :]
+    _assert_same(_run_pertensor(fl, x), x)
+
+
+def test_cast_sweep_sampled():
+    """All fp32 patterns of selected exponent ranges (subnormals, the E4M3
+    subnormal/normal boundary, the saturation range) plus a random sample."""
+    fl = lib()
+    for top in (0x00, 0x3A, 0x3B, 0x3C, 0x3D, 0x43, 0x80, 0xBB, 0xC3, 0x7F, 0xFF):
+        lo = np.uint64(top) << np.uint64(24)
+        bits = (np.arange(1 << 24, dtype=np.uint64) + lo).astype(np.uint32)
+        _sweep_chunk(fl, bits)
+    rng = np.random.default_rng(99)
+    _sweep_chunk(fl, rng.integers(0, 2 ** 32, size=1 << 24, dtype=np.uint64).astype(np.uint32))
+
+
+@pytest.mark.skipif(os.environ.get("FP8LA_EXHAUSTIVE") != "1",
+                    reason="set FP8LA_EXHAUSTIVE=1 for the full 2^32 sweep")
+def test_cast_sweep_exhaustive():
+    fl = lib()
+    for top in range(256):
+        lo = np.uint64(top) << np.uint64(24)
+        _sweep_chunk(fl, (np.arange(1 << 24, dtype=np.uint64) + lo).astype(np.uint32))
+
+
+@pytest.mark.parametrize("shape,pad", [((64, 64), 0), ((70, 100), 0), ((33, 31), 5),
+                                       ((96, 4096), 8), ((1, 1), 0), ((257, 129), 3)])
+def test_blockwise_32x32(shape, pad):
+    import torch
+    fl = lib()
+    rng = np.random.default_rng(shape[0] * 1000 + shape[1])
+    x = (rng.standard_normal(shape) * rng.choice([0.01, 1, 100], size=shape)).astype(np.float32)
+    x[0, 0] = 77.0
+    rows, cols = shape
+    xs = torch.zeros((rows, cols + pad), dtype=torch.float32, device="cuda")
+    xs[:, :cols] = to_dev(x)
+    q, s = fl.quantize_blockwise_32x32(xs[:, :cols])
+    torch.cuda.synchronize()
+    rq, rs = oracle.quantize_blockwise_32x32(x)
+    assert np.array_equal(q.cpu().numpy(), rq)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+
+
+def test_blockwise_transformer_weights_sampled():
+    """gate_up weights [57344][8192] ~ N(0,0.02): full GPU pass, oracle on
+    sampled 32-aligned tile regions."""
+    import torch
+    fl = lib()
+    X, W = workloads.transformer_linear("gate_up", seed=0, tokens=64)
+    q, s = fl.quantize_blockwise_32x32(to_dev(W))
+    torch.cuda.synchronize()
+    qn, sn = q.cpu().numpy(), s.cpu().numpy()
+    rng = np.random.default_rng(5)
+    for _ in range(8):
+        r0 = int(rng.integers(0, W.shape[0] // 32 - 2)) * 32
+        c0 = int(rng.integers(0, W.shape[1] // 32 - 2)) * 32
+        rq, rs = oracle.quantize_blockwise_32x32(W[r0:r0 + 64, c0:c0 + 64])
+        assert np.array_equal(qn[r0:r0 + 64, c0:c0 + 64], rq)
+        assert np.array_equal(sn[r0 // 32:r0 // 32 + 2, c0 // 32:c0 // 32 + 2], rs)
