@@ -1,0 +1,122 @@
+"""GPU parity: grouped (MoE) E4M3 GEMM against the oracle, per group within
+the per-tensor bound with that group's scales; rows outside every group are
+left untouched."""
+
+import numpy as np
+import pytest
+
+import oracle
+from _helpers import bf16_to_f64, check_pertensor, lib, random_codes, to_dev
+from precision_linear_algebra_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def _grouped(fl, A, offs, B, sa, sb, cap_extra=0):
+    import torch
+    cap = A.shape[0] + cap_extra
+    K = A.shape[1]
+    E, N, _ = B.shape
+    kp = max(16, (K + 15) // 16 * 16)
+    dA = torch.zeros((cap, kp), dtype=torch.uint8, device="cuda")
+    dA[:A.shape[0], :K] = to_dev(A)
+    dB = torch.zeros((E, N, kp), dtype=torch.uint8, device="cuda")
+    dB[:, :, :K] = to_dev(B)
+    dC = torch.full((cap, N), 3.0, dtype=torch.bfloat16, device="cuda")
+    d_off = to_dev(np.asarray(offs, np.int32))
+    d_sa = to_dev(np.asarray(sa, np.float32))
+    d_sb = to_dev(np.asarray(sb, np.float32))
+    fl.fp8_grouped_gemm(E, d_off.data_ptr(), cap, dA.data_ptr(), kp, dB.data_ptr(), kp,
+                        N * kp, dC.data_ptr(), N, N, K, d_sa.data_ptr(), d_sb.data_ptr(),
+                        torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert fl.device_status() == 0
+    return bf16_to_f64(dC)
+
+
+@pytest.mark.parametrize("counts,N,K", [
+    ([7, 0, 300, 0, 129], 512, 256),
+    ([128, 128], 256, 128),
+    ([0, 0, 1], 96, 48),
+    ([1000], 600, 200),
+    ([5, 17, 250, 3, 0, 0, 140, 77], 272, 160),
+])
+def test_grouped_random_codes(counts, N, K):
+    fl = lib()
+    rng = np.random.default_rng(sum(counts) + N + K)
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    E = len(counts)
+    A = random_codes(rng, (int(offs[-1]), K))
+    B = random_codes(rng, (E, N, K))
+    sa = rng.uniform(0.01, 2, E).astype(np.float32)
+    sb = rng.uniform(0.01, 2, E).astype(np.float32)
+    got = _grouped(fl, A, offs, B, sa, sb, cap_extra=37)
+    for e in range(E):
+        lo, hi = offs[e], offs[e + 1]
+        if hi > lo:
+            check_pertensor(got[lo:hi], A[lo:hi], B[e], sa[e], sb[e], what="group %d" % e)
+    assert np.all(got[offs[-1]:] == 3.0), "rows past the last group were written"
+
+
+def test_grouped_equals_per_group_gemm_calls():
+    """One grouped launch equals E separate fp8_gemm calls, bit for bit."""
+    import torch
+    fl = lib()
+    rng = np.random.default_rng(12)
+    counts = [200, 0, 64, 333]
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    N, K = 512, 384
+    A = random_codes(rng, (int(offs[-1]), K))
+    B = random_codes(rng, (4, N, K))
+    sa = rng.uniform(0.1, 1, 4).astype(np.float32)
+    sb = rng.uniform(0.1, 1, 4).astype(np.float32)
+    got = _grouped(fl, A, offs, B, sa, sb)
+    for e in range(4):
+        lo, hi = offs[e], offs[e + 1]
+        if hi == lo:
+            continue
+        C = fl.gemm(to_dev(A[lo:hi]), to_dev(B[e]), to_dev(sa[e:e + 1]), to_dev(sb[e:e + 1]))
+        torch.cuda.synchronize()
+        assert np.array_equal(bf16_to_f64(C), got[lo:hi])
+
+
+def test_moe_layer_full_size_sampled():
+    """8 experts, K 4096, N 14336, 16384 routed rows with Dirichlet counts;
+    per-expert per-tensor quantisation on the GPU, one grouped launch; the
+    oracle checks sampled rows of every group against sampled columns."""
+    import torch
+    fl = lib()
+    counts, offs, X, W = workloads.moe_layer(seed=0)
+    E, N, K = W.shape
+    dX = to_dev(X)
+    dW = to_dev(W)
+    qx = torch.empty(X.shape, dtype=torch.uint8, device="cuda")
+    qw = torch.empty(W.shape, dtype=torch.uint8, device="cuda")
+    amax = torch.empty(2 * E, dtype=torch.float32, device="cuda")
+    sx = torch.empty(E, dtype=torch.float32, device="cuda")
+    sw = torch.empty(E, dtype=torch.float32, device="cuda")
+    for e in range(E):
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        fl.quantize_pertensor(dX[lo:hi], q=qx[lo:hi], amax=amax[e:e + 1], scale=sx[e:e + 1])
+        fl.quantize_pertensor(dW[e], q=qw[e], amax=amax[E + e:E + e + 1], scale=sw[e:e + 1])
+    C = fl.grouped_gemm(to_dev(offs), qx, qw, sx, sw)
+    torch.cuda.synchronize()
+    assert fl.device_status() == 0
+    qx_n, qw_n, sx_n, sw_n = qx.cpu().numpy(), qw.cpu().numpy(), sx.cpu().numpy(), sw.cpu().numpy()
+    Cn = bf16_to_f64(C)
+    rng = np.random.default_rng(1)
+    cols = np.sort(rng.choice(N, 96, replace=False))
+    for e in range(E):
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        if hi == lo:
+            continue
+        rq, _, rs = oracle.quantize_pertensor(X[lo:hi])
+        assert np.array_equal(qx_n[lo:hi], rq) and sx_n[e] == rs
+        # weights: the oracle's amax and scales on the whole expert, its
+        # cast on the sampled rows only (the cast is elementwise)
+        qs, ws = oracle.scales_from_amax(oracle.amax_fp32(W[e]))
+        assert sw_n[e] == ws
+        assert np.array_equal(qw_n[e][cols], oracle.encode((W[e][cols] * qs).astype(np.float32)))
+        rows = np.sort(rng.choice(hi - lo, min(48, hi - lo), replace=False))
+        check_pertensor(Cn[lo + rows][:, cols], qx_n[lo:hi], qw_n[e], sx_n[e], sw_n[e],
+                        rows=rows, cols=cols, what="expert %d" % e)
