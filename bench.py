@@ -217,11 +217,166 @@ def _cpu_baseline_subprocess():
 
 
 # ------------------------------------------------------------------ GPU arm
+class _Phases:
+    """CUDA events around the phases of a step ('quant', 'gemm'), on the
+    launching stream; durations are summed per phase per step."""
+
+    def __init__(self, torch, stream):
+        self.torch, self.stream = torch, stream
+        self.events = []
+        self.on = False
+
+    def mark(self, phase):
+        if self.on:
+            e = self.torch.cuda.Event(enable_timing=True)
+            e.record(self.stream)
+            self.events.append((phase, e))
+
+    def collect(self):
+        out = {}
+        for (ph, e0), (_, e1) in zip(self.events[0::2], self.events[1::2]):
+            out[ph] = out.get(ph, 0.0) + e0.elapsed_time(e1)
+        self.events = []
+        return out
+
+
+def _workload_pertensor(fl, torch, dev, sptr, ph):
+    from precision_linear_algebra_gb300 import workloads
+    A_np, B_np = workloads.square_outliers(N_SIZE, seed=0)
+    A = torch.from_numpy(A_np).to(dev)
+    B = torch.from_numpy(B_np).to(dev)
+    qa = torch.empty((N_SIZE, N_SIZE), dtype=torch.uint8, device=dev)
+    qb = torch.empty_like(qa)
+    amax = torch.empty(2, dtype=torch.float32, device=dev)
+    scale = torch.empty(2, dtype=torch.float32, device=dev)
+    C = torch.empty((N_SIZE, N_SIZE), dtype=torch.bfloat16, device=dev)
+    P = lambda t, i=0: t.data_ptr() + i * t.element_size()
+
+    def step():
+        ph.mark("quant")
+        fl.fp8_quantize_pertensor(P(A), N_SIZE, N_SIZE, N_SIZE, P(qa), N_SIZE,
+                                  P(amax, 0), P(scale, 0), sptr)
+        fl.fp8_quantize_pertensor(P(B), N_SIZE, N_SIZE, N_SIZE, P(qb), N_SIZE,
+                                  P(amax, 1), P(scale, 1), sptr)
+        ph.mark("quant")
+        ph.mark("gemm")
+        fl.fp8_gemm(P(qa), N_SIZE, P(qb), N_SIZE, P(C), N_SIZE, N_SIZE, N_SIZE, N_SIZE,
+                    P(scale, 0), P(scale, 1), sptr)
+        ph.mark("gemm")
+
+    return dict(step=step, flops=FLOPS, launches=5, workload=WORKLOAD,
+                config={"M": N_SIZE, "N": N_SIZE, "K": N_SIZE,
+                        "l2": "inputs 2 x 268 MB fp32 > 129 MB L2; no flush"},
+                inputs=[(A, A_np), (B, B_np)], outputs=[C],
+                quant_elems=2 * N_SIZE * N_SIZE, gemm_label="gemm_e4m3_kernel<256,4,false>",
+                gemm_bytes=GEMM_BYTES, profile=("gemm_e4m3_pertensor_8192", GEMM_SOURCES),
+                qprofile=("quantize_pertensor_8192", QUANT_SOURCES))
+
+
+def _workload_blockscaled(fl, torch, dev, sptr, ph):
+    from precision_linear_algebra_gb300 import workloads
+    items = []
+    flops = 0.0
+    qelems = 0
+    gbytes = 0
+    for name in ("qkv", "attn_out", "gate_up", "down"):
+        X_np, W_np = workloads.transformer_linear(name, seed=0)
+        M, K = X_np.shape
+        N = W_np.shape[0]
+        X = torch.from_numpy(X_np).to(dev)
+        W = torch.from_numpy(W_np).to(dev)
+        qx = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        qw = torch.empty((N, K), dtype=torch.uint8, device=dev)
+        sx = torch.empty(((M + 31) // 32, (K + 31) // 32), dtype=torch.float32, device=dev)
+        sw = torch.empty(((N + 31) // 32, (K + 31) // 32), dtype=torch.float32, device=dev)
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        items.append((M, N, K, X, W, qx, qw, sx, sw, C, X_np, W_np))
+        flops += 2.0 * M * N * K
+        qelems += M * K + N * K
+        gbytes += M * K + N * K + 2 * M * N + 4 * (sx.numel() + sw.numel())
+
+    def step():
+        for (M, N, K, X, W, qx, qw, sx, sw, C, _, _) in items:
+            ph.mark("quant")
+            fl.fp8_quantize_blockwise_32x32(X.data_ptr(), M, K, K, qx.data_ptr(), K,
+                                            sx.data_ptr(), sx.stride(0), sptr)
+            fl.fp8_quantize_blockwise_32x32(W.data_ptr(), N, K, K, qw.data_ptr(), K,
+                                            sw.data_ptr(), sw.stride(0), sptr)
+            ph.mark("quant")
+            ph.mark("gemm")
+            fl.fp8_gemm_blockscaled_32x32(qx.data_ptr(), K, qw.data_ptr(), K, C.data_ptr(), N,
+                                          M, N, K, sx.data_ptr(), sx.stride(0),
+                                          sw.data_ptr(), sw.stride(0), sptr)
+            ph.mark("gemm")
+
+    return dict(step=step, flops=flops, launches=12,
+                workload=("32x32 block-scaled E4M3: block-quantize activations [4096][K] ~ N(0,1) "
+                          "and weights [N][K] ~ N(0,0.02), then the block-scaled GEMM, for the "
+                          "four 70B-class linears qkv (10240,8192), attn_out (8192,8192), gate_up "
+                          "(57344,8192), down (8192,28672); seed 0"),
+                config={"M": 4096, "linears": "qkv,attn_out,gate_up,down",
+                        "l2": "inputs 4.3 GB fp32 > 129 MB L2; no flush"},
+                inputs=[(it[3], it[10]) for it in items] + [(it[4], it[11]) for it in items],
+                outputs=[it[9] for it in items], quant_elems=qelems,
+                gemm_label="gemm_e4m3_block32_kernel", gemm_bytes=gbytes,
+                profile=("gemm_e4m3_block32_transformer", ["precision_linear_algebra_gb300/csrc/gemm_block32.cu",
+                                                           "precision_linear_algebra_gb300/csrc/ptx.cuh"]),
+                qprofile=("quantize_block32_transformer", QUANT_SOURCES))
+
+
+def _workload_grouped(fl, torch, dev, sptr, ph):
+    from precision_linear_algebra_gb300 import workloads
+    counts, offs, X_np, W_np = workloads.moe_layer(seed=0)
+    E, N, K = W_np.shape
+    Mt = int(offs[-1])
+    X = torch.from_numpy(X_np).to(dev)
+    W = torch.from_numpy(W_np).to(dev)
+    qx = torch.empty((Mt, K), dtype=torch.uint8, device=dev)
+    qw = torch.empty((E, N, K), dtype=torch.uint8, device=dev)
+    amax = torch.empty(2 * E, dtype=torch.float32, device=dev)
+    sx = torch.empty(E, dtype=torch.float32, device=dev)
+    sw = torch.empty(E, dtype=torch.float32, device=dev)
+    d_off = torch.from_numpy(offs.astype("int32")).to(dev)
+    C = torch.empty((Mt, N), dtype=torch.bfloat16, device=dev)
+    P = lambda t, i=0: t.data_ptr() + i * t.element_size()
+    offs_l = [int(v) for v in offs]
+
+    def step():
+        ph.mark("quant")
+        for e in range(E):
+            lo, hi = offs_l[e], offs_l[e + 1]
+            fl.fp8_quantize_pertensor(P(X) + lo * K * 4, hi - lo, K, K, P(qx) + lo * K, K,
+                                      P(amax, e), P(sx, e), sptr)
+            fl.fp8_quantize_pertensor(P(W) + e * N * K * 4, N, K, K, P(qw) + e * N * K, K,
+                                      P(amax, E + e), P(sw, e), sptr)
+        ph.mark("quant")
+        ph.mark("gemm")
+        fl.fp8_grouped_gemm(E, d_off.data_ptr(), Mt, P(qx), K, P(qw), K, N * K, P(C), N, N, K,
+                            P(sx), P(sw), sptr)
+        ph.mark("gemm")
+
+    return dict(step=step, flops=2.0 * Mt * N * K, launches=4 * E + 1,
+                workload=("grouped MoE E4M3: 8 experts, K 4096, N 14336, 8192 tokens top-2 "
+                          "(16384 rows, Dirichlet(1) counts %s), per-expert per-tensor quantize "
+                          "of activations and weights, one grouped GEMM launch; seed 0"
+                          % list(map(int, counts))),
+                config={"experts": E, "N": N, "K": K, "rows": Mt,
+                        "l2": "inputs 2.1 GB fp32 > 129 MB L2; no flush"},
+                inputs=[(X, X_np), (W, W_np)], outputs=[C], quant_elems=Mt * K + E * N * K,
+                gemm_label="gemm_e4m3_kernel<256,4,true>",
+                gemm_bytes=Mt * K + E * N * K + 2 * Mt * N,
+                profile=("gemm_e4m3_grouped_moe", GEMM_SOURCES),
+                qprofile=("quantize_pertensor_8192", QUANT_SOURCES))
+
+
+WORKLOADS = {"pertensor8192": _workload_pertensor, "blockscaled": _workload_blockscaled,
+             "grouped": _workload_grouped}
+
+
 def run_gpu(args):
-    import numpy as np
     import torch
     import precision_linear_algebra_gb300 as fl
-    from precision_linear_algebra_gb300 import build, workloads
+    from precision_linear_algebra_gb300 import build
 
     world, rank, local_rank = _dist_env()
     if world > 1:
@@ -234,37 +389,11 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     fl.load()
-
-    A_np, B_np = workloads.square_outliers(N_SIZE, seed=0)
-    A = torch.from_numpy(A_np).to(dev)
-    B = torch.from_numpy(B_np).to(dev)
-    qa = torch.empty((N_SIZE, N_SIZE), dtype=torch.uint8, device=dev)
-    qb = torch.empty_like(qa)
-    amax = torch.empty(2, dtype=torch.float32, device=dev)
-    scale = torch.empty(2, dtype=torch.float32, device=dev)
-    C = torch.empty((N_SIZE, N_SIZE), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
-    P = lambda t, i=0: t.data_ptr() + i * t.element_size()
-
-    ev_q = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    ev_g = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    q_ms, g_ms = [], []
-
-    def step(record=False):
-        if record:
-            ev_q[0].record(stream)
-        fl.fp8_quantize_pertensor(P(A), N_SIZE, N_SIZE, N_SIZE, P(qa), N_SIZE,
-                                  P(amax, 0), P(scale, 0), sptr)
-        fl.fp8_quantize_pertensor(P(B), N_SIZE, N_SIZE, N_SIZE, P(qb), N_SIZE,
-                                  P(amax, 1), P(scale, 1), sptr)
-        if record:
-            ev_q[1].record(stream)
-            ev_g[0].record(stream)
-        fl.fp8_gemm(P(qa), N_SIZE, P(qb), N_SIZE, P(C), N_SIZE, N_SIZE, N_SIZE, N_SIZE,
-                    P(scale, 0), P(scale, 1), sptr)
-        if record:
-            ev_g[1].record(stream)
+    ph = _Phases(torch, stream)
+    W = WORKLOADS[args.workload](fl, torch, dev, sptr, ph)
+    step = W["step"]
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -272,12 +401,16 @@ def run_gpu(args):
     if fl.fp8_get_device_status(sptr) != 0:
         raise RuntimeError("device status reports a timeout during warm-up")
 
-    # Per-kernel durations, measured live on the launching stream.
+    # Per-phase kernel durations, measured live on the launching stream.
+    q_ms, g_ms = [], []
+    ph.on = True
     for _ in range(min(args.steps, 50)):
-        step(record=True)
+        step()
         torch.cuda.synchronize()
-        q_ms.append(ev_q[0].elapsed_time(ev_q[1]))
-        g_ms.append(ev_g[0].elapsed_time(ev_g[1]))
+        d = ph.collect()
+        q_ms.append(d["quant"])
+        g_ms.append(d["gemm"])
+    ph.on = False
 
     visible = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v]
     sampler = ClockSampler(visible[local_rank] if local_rank < len(visible) else local_rank)
@@ -304,20 +437,20 @@ def run_gpu(args):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms_total = tt.item()
     ms_step = ms_total / args.steps
-    value = world * FLOPS / (ms_step * 1e-3) / 1e12
+    value = world * W["flops"] / (ms_step * 1e-3) / 1e12
 
     # End to end through the public API, host buffers: pinned H2D of the
-    # step's fp32 inputs, the three calls, D2H of C, every step.
-    A_h = torch.from_numpy(A_np).pin_memory()
-    B_h = torch.from_numpy(B_np).pin_memory()
-    C_h = torch.empty((N_SIZE, N_SIZE), dtype=torch.bfloat16).pin_memory()
+    # step's fp32 inputs, the step's calls, D2H of the outputs, every step.
+    hosts = [(d, torch.from_numpy(h).pin_memory()) for d, h in W["inputs"]]
+    outs = [(o, torch.empty(o.shape, dtype=o.dtype).pin_memory()) for o in W["outputs"]]
     e2e_steps = max(3, min(args.steps, 30))
 
     def e2e_step():
-        A.copy_(A_h, non_blocking=True)
-        B.copy_(B_h, non_blocking=True)
+        for d, h in hosts:
+            d.copy_(h, non_blocking=True)
         step()
-        C_h.copy_(C, non_blocking=True)
+        for o, h in outs:
+            h.copy_(o, non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -334,14 +467,17 @@ def run_gpu(args):
         tt = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = tt.item()
+    h2d = sum(h.numel() * h.element_size() for _, h in hosts)
+    d2h = sum(h.numel() * h.element_size() for _, h in outs)
 
     hbm, bf16_burst, bf16_sust, peak_src = _peaks()
     fp8_peak = bf16_burst * FP8_OVER_BF16
     g_avg = statistics.mean(g_ms)
-    q_avg = statistics.mean(q_ms) / 2.0          # per operand
-    gemm_tflops = FLOPS / (g_avg * 1e-3) / 1e12
-    quant_gbs = QUANT_BYTES_PER_ELEM * N_SIZE * N_SIZE / (q_avg * 1e-3) / 1e9
-    traffic = _profile_traffic("gemm_e4m3_pertensor_8192", GEMM_SOURCES)
+    q_avg = statistics.mean(q_ms)
+    gemm_tflops = W["flops"] / (g_avg * 1e-3) / 1e12
+    quant_gbs = QUANT_BYTES_PER_ELEM * W["quant_elems"] / (q_avg * 1e-3) / 1e9
+    if args.workload == "blockscaled":
+        quant_gbs = 5 * W["quant_elems"] / (q_avg * 1e-3) / 1e9   # one pass: 4 B read + 1 B written
 
     if rank == 0:
         line = {
@@ -349,32 +485,33 @@ def run_gpu(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3 (fp32 accumulate, bf16 out)", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "M": N_SIZE, "N": N_SIZE, "K": N_SIZE,
-                       "parallelism": "replicas" if world > 1 else "single GPU",
-                       "l2": "inputs 2 x 268 MB fp32 > 129 MB L2; no flush"},
+            "config": dict({"workload": W["workload"],
+                            "parallelism": "replicas" if world > 1 else "single GPU"},
+                           **W["config"]),
             "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak,
                          "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak,
-                         "traffic": traffic,
-                         "kernel": "gemm_e4m3_kernel<256,4,false>",
+                         "traffic": _profile_traffic(*W["profile"]),
+                         "kernel": W["gemm_label"],
                          "peak_source": "%s bf16 burst %.1f x nominal fp8/bf16 ratio 2"
                                         % (peak_src, bf16_burst),
                          "frac_of_sustained": (gemm_tflops / (bf16_sust * FP8_OVER_BF16)
                                                if bf16_sust else None)},
             "roofline_quantize": {"bound": "hbm", "achieved": quant_gbs, "peak": hbm,
                                   "unit": "GB/s", "frac": quant_gbs / hbm,
-                                  "traffic": _profile_traffic("quantize_pertensor_8192",
-                                                              QUANT_SOURCES),
-                                  "algorithmic_bytes_per_elem": QUANT_BYTES_PER_ELEM},
-            "breakdown": {"gemm_ms": g_avg, "quantize_ms_per_operand": q_avg,
+                                  "traffic": _profile_traffic(*W["qprofile"]),
+                                  "algorithmic_bytes_per_elem":
+                                      5 if args.workload == "blockscaled" else QUANT_BYTES_PER_ELEM},
+            "breakdown": {"gemm_ms": g_avg, "quantize_ms": q_avg,
                           "gemm_tflops": gemm_tflops, "quantize_gbs": quant_gbs},
-            "e2e": {"value": world * FLOPS / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": 2 * 4 * N_SIZE * N_SIZE,
-                    "d2h_bytes_per_step": 2 * N_SIZE * N_SIZE,
+            "e2e": {"value": world * W["flops"] / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms},
-            "gpu_launches": 5 * args.steps,
+            "gpu_launches": W["launches"] * args.steps,
             "clocks": clocks,
         }
-        if not args.no_cpu_baseline:
+        if args.workload != "pertensor8192":
+            line["workload_kind"] = args.workload
+        if not args.no_cpu_baseline and args.workload == "pertensor8192":
             line["cpu_baseline"] = _cpu_baseline_subprocess()
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -388,6 +525,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="pertensor8192", choices=sorted(WORKLOADS),
+                    help="pertensor8192 is the headline line; the others measure the "
+                         "block-scaled and grouped variants")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

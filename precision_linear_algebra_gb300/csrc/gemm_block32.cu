@@ -1,12 +1,433 @@
-// 32x32 block-scaled E4M3 GEMM (tcgen05 partials + CUDA-core promotion).
+// 32x32 block-scaled E4M3 GEMM: tcgen05 partial sums per 32-wide K block,
+// promoted into FP32 register accumulators on the CUDA cores.
+//
+// Method: [P3] "JAX 中使用 Triton 优化 Blackwell GPU 的 FP8 GEMM 内核",
+// implementation paragraph (one scale per 32x32 block, "microscaling") and
+// warp-specialisation paragraph (one warp loads by TMA, one issues the FP8
+// MMA, a third promotes on the CUDA cores); output rule of [P1]
+// "通过 CUTLASS 命名约定在 Triton 中实现 FP8 GEMM 内核" (FP32 accumulator,
+// BF16 output).
+//
+//   C[m][n] = bf16( sum_kb sa[m/32][kb] * sb[n/32][kb] * S_kb[m][n] )
+//
+// The tile scales are arbitrary fp32 values, so they cannot be folded into
+// the tensor-core instruction; each 32-wide K block's product S_kb is formed
+// by one tcgen05.mma (M=128, N=128, K=32) into a fresh TMEM buffer and then
+// weighted and added on the CUDA cores.
+//
+// Design (one CTA per SM, persistent, 10 warps):
+//   * warp 8: producer.  Lane 0 issues the TMA loads of a 128 x 128 A tile
+//     and a 128 x 128 B tile per 128-wide K stage (6-stage ring); all 32
+//     lanes fetch the stage's 16 A-tile and 16 B-tile scales (4 row tiles x
+//     4 K blocks each) into shared memory beside it.
+//   * warp 9: MMA issuer (lane 0).  One MMA per 32-wide K block into one of
+//     four 128-column TMEM partial buffers (`pfull` / `pempty` ring).
+//   * warps 0-7: promotion.  Warp w reads TMEM lanes 32(w%4).. (C rows) and
+//     columns 64(w/4)..+63; each thread keeps its row's 64 FP32
+//     accumulators in registers and, for every K block, adds
+//     (sa*sb) * partial with packed FP32 FMAs (fma.rn.f32x2).  The scale is
+//     uniform over a warp's 32 x 32 chunk.  After the last K block it
+//     rounds to BF16 and stores.
+//   * A stage is recycled only when its MMAs have completed and all eight
+//     promotion warps have read its scales (empty barrier count 1 + 8).
+#include <cuda_bf16.h>
+
 #include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8la {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int BK = 128;          // K per stage (bytes = E4M3 values)
+constexpr int KB = 32;           // scale block along K, = K per MMA
+constexpr int STAGES = 6;
+constexpr int NPART = 4;         // TMEM partial buffers of BN columns
+constexpr int kPromoWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr int GROUP_M = 16;
+constexpr int kTmemCols = NPART * BN;  // 512
+
+struct BsArgs {
+  uint16_t *C;
+  int64_t ldc;
+  int32_t M, N, K;
+  const float *sa;
+  int64_t ld_sa;
+  const float *sb;
+  int64_t ld_sb;
+  unsigned *status;
+  uint64_t timeout_ns;
+  int32_t c_vec16;
+};
+
+struct Lay {
+  static constexpr int kABytes = BM * BK;
+  static constexpr int kBBytes = BN * BK;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kA = 0;
+  static constexpr int kB = kA + STAGES * kABytes;
+  static constexpr int kScale = kB + STAGES * kBBytes;     // STAGES x 32 floats
+  static constexpr int kBar = kScale + STAGES * 32 * 4;
+  static constexpr int kNumBars = 2 * STAGES + 2 * NPART + 1;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kEnd = kMisc + 16;
+  static constexpr int kAlloc = kEnd + 1024;
+};
+
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n,
+                                            int &mb, int &nb) {
+  const int per_group = GROUP_M * tiles_n;
+  const int g = t / per_group;
+  const int first_m = g * GROUP_M;
+  const int gm = min(tiles_m - first_m, GROUP_M);
+  const int r = t - g * per_group;
+  mb = first_m + r % gm;
+  nb = r / gm;
+}
+
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// acc = s * p + acc, two lanes at once, each rounded once.
+__device__ __forceinline__ void fma2(uint64_t &acc, uint64_t s, uint64_t p) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(s), "l"(p));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_e4m3_block32_kernel(const __grid_constant__ CUtensorMap tmA,
+                             const __grid_constant__ CUtensorMap tmB,
+                             const BsArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t *sbase = smem_raw + (base - raw_addr);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const uint32_t bar0 = base + Lay::kBar;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto pfull_bar = [&](int p) { return bar0 + 8u * (2 * STAGES + p); };
+  auto pempty_bar = [&](int p) { return bar0 + 8u * (2 * STAGES + NPART + p); };
+  const uint32_t final_bar = bar0 + 8u * (2 * STAGES + 2 * NPART);
+  float *scales = reinterpret_cast<float *>(sbase + Lay::kScale);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + Lay::kMisc);
+  volatile int *abort_flag =
+      reinterpret_cast<volatile int *>(sbase + Lay::kMisc + 4);
+
+  const int tiles_m = (a.M + BM - 1) / BM;
+  const int tiles_n = (a.N + BN - 1) / BN;
+  const int total_tiles = tiles_m * tiles_n;
+  const int nks = (a.K + BK - 1) / BK;          // stages per tile
+  const int nkb = (a.K + KB - 1) / KB;          // scale blocks along K
+  const int srow_a = (a.M + 31) / 32, srow_b = (a.N + 31) / 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1 + kPromoWarps);
+    }
+    for (int p = 0; p < NPART; ++p) {
+      mbar_init(pfull_bar(p), 1);
+      mbar_init(pempty_bar(p), kPromoWarps);
+    }
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    uint32_t s = 0, ph = 0, issued = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+      int mb, nb;
+      tile_coords(t, tiles_m, tiles_n, mb, nb);
+      const int m0 = mb * BM, n0 = nb * BN;
+      for (int ks = 0; ks < nks; ++ks) {
+        const bool ready = mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns,
+                                     a.status, abort_flag);
+        if (!__all_sync(0xffffffffu, ready)) {
+          ok = false;
+          break;
+        }
+        // Lane l < 16: sa of row tile m0/32 + (l & 3), K block 4ks + (l >> 2);
+        // lane l >= 16: the same for sb and column tiles.
+        const int i = lane & 3, j = (lane >> 2) & 3;
+        const int kb = ks * 4 + j;
+        float v = 0.0f;
+        if (lane < 16) {
+          const int rt = m0 / 32 + i;
+          if (rt < srow_a && kb < nkb) v = a.sa[rt * a.ld_sa + kb];
+        } else {
+          const int ct = n0 / 32 + i;
+          if (ct < srow_b && kb < nkb) v = a.sb[ct * a.ld_sb + kb];
+        }
+        scales[s * 32 + lane] = v;
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full_bar(s), Lay::kStageBytes);
+          tma_load_2d(base + Lay::kA + s * Lay::kABytes, &tmA, full_bar(s),
+                      ks * BK, m0);
+          tma_load_2d(base + Lay::kB + s * Lay::kBBytes, &tmB, full_bar(s),
+                      ks * BK, n0);
+        }
+        ++issued;
+        if (++s == STAGES) { s = 0; ph ^= 1u; }
+      }
+    }
+    if (lane == 0) {
+      for (uint32_t st = 0; st < STAGES; ++st) {
+        if (issued <= st) break;
+        const uint32_t arms = (issued - 1 - st) / STAGES + 1;
+        mbar_wait_drain(full_bar(st), (arms - 1) & 1u, a.timeout_ns, a.status);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+      uint32_t s = 0, ph = 0, p = 0, pph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        for (int ks = 0; ok && ks < nks; ++ks) {
+          if (!mbar_wait(full_bar(s), ph, a.timeout_ns, a.status,
+                         abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc =
+              smem_desc_k128_sw128(base + Lay::kA + s * Lay::kABytes);
+          const uint64_t bdesc =
+              smem_desc_k128_sw128(base + Lay::kB + s * Lay::kBBytes);
+          for (int k = 0; k < BK / KB; ++k) {
+            if (!mbar_wait(pempty_bar(p), pph ^ 1u, a.timeout_ns, a.status,
+                           abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            umma_f8f6f4(tmem_base + p * BN, adesc + 2u * k, bdesc + 2u * k,
+                        idesc, 0u);
+            umma_commit(pfull_bar(p));
+            if (++p == NPART) { p = 0; pph ^= 1u; }
+          }
+          if (!ok) break;
+          umma_commit(empty_bar(s));
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+      }
+      umma_commit(final_bar);
+      mbar_wait_drain(final_bar, 0, a.timeout_ns, a.status);
+    }
+  } else {
+    // ----------------------------------------------------------- promotion
+    const int q = warp & 3;          // TMEM lane quarter = 32-row tile
+    const int h = warp >> 2;         // column half: 64h .. 64h + 63
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    uint32_t s = 0, ph = 0, p = 0, pph = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+      int mb, nb;
+      tile_coords(t, tiles_m, tiles_n, mb, nb);
+      uint64_t acc[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) acc[j] = 0;
+      for (int ks = 0; ok && ks < nks; ++ks) {
+        // Acquire the producer's scale writes for this stage.
+        const bool sready = mbar_wait(full_bar(s), ph, a.timeout_ns,
+                                      a.status, abort_flag);
+        if (!__all_sync(0xffffffffu, sready)) {
+          ok = false;
+          break;
+        }
+        const float *sc = scales + s * 32;
+#pragma unroll 1
+        for (int k = 0; k < BK / KB; ++k) {
+          const float sav = sc[k * 4 + q];
+          const float s0 = __fmul_rn(sav, sc[16 + k * 4 + 2 * h]);
+          const float s1 = __fmul_rn(sav, sc[16 + k * 4 + 2 * h + 1]);
+          const bool pready = mbar_wait(pfull_bar(p), pph, a.timeout_ns,
+                                        a.status, abort_flag);
+          if (!__all_sync(0xffffffffu, pready)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t taddr = tmem_base + lane_base + p * BN + 64 * h;
+          uint32_t r[32];
+          tmem_ld32(taddr, r);
+          const uint64_t s0x2 = pack2(s0, s0);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            fma2(acc[j], s0x2, pack2(__uint_as_float(r[2 * j]),
+                                     __uint_as_float(r[2 * j + 1])));
+          tmem_ld32(taddr + 32, r);
+          const uint64_t s1x2 = pack2(s1, s1);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            fma2(acc[16 + j], s1x2, pack2(__uint_as_float(r[2 * j]),
+                                          __uint_as_float(r[2 * j + 1])));
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(pempty_bar(p));
+          if (++p == NPART) { p = 0; pph ^= 1u; }
+        }
+        if (!ok) break;
+        // This warp is done with the stage's scales.
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(s));
+        if (++s == STAGES) { s = 0; ph ^= 1u; }
+      }
+      if (!ok) break;
+      // Epilogue: round to BF16 and store this thread's 64 columns.
+      const int row = mb * BM + q * 32 + lane;
+      const int n = nb * BN + 64 * h;
+      if (row < a.M && n < a.N) {
+        uint16_t *crow = a.C + static_cast<int64_t>(row) * a.ldc;
+        uint32_t w[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          float lo, hi;
+          unpack2(acc[j], lo, hi);
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+          w[j] = *reinterpret_cast<const uint32_t *>(&b2);
+        }
+        if (a.c_vec16 && n + 64 <= a.N) {
+          uint4 *dst = reinterpret_cast<uint4 *>(crow + n);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2],
+                                w[4 * j + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            if (n + j < a.N)
+              crow[n + j] = static_cast<uint16_t>(
+                  (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+__global__ void zero_c_kernel_bs(uint16_t *C, int64_t ldc, int64_t M,
+                                 int64_t N) {
+  const int64_t n = M * N;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       i < n; i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / N, c = i - r * N;
+    C[r * ldc + c] = 0;
+  }
+}
+
+bool encode_2d_bs(CUtensorMap *m, const void *ptr, uint64_t inner,
+                  uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                  uint32_t box_outer) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims,
+             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace fp8la
+
+using namespace fp8la;
 
 extern "C" fp8la_status fp8_gemm_blockscaled_32x32(
     const uint8_t *A, int64_t lda, const uint8_t *B, int64_t ldb, uint16_t *C,
     int64_t ldc, int64_t M, int64_t N, int64_t K, const float *sa,
     int64_t ld_sa, const float *sb, int64_t ld_sb, fp8la_stream_t stream) {
-  (void)A; (void)lda; (void)B; (void)ldb; (void)C; (void)ldc; (void)M;
-  (void)N; (void)K; (void)sa; (void)ld_sa; (void)sb; (void)ld_sb;
-  (void)stream;
-  return FP8LA_ERR_UNSUPPORTED;
+  if (M < 0 || N < 0 || K < 0) return FP8LA_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return FP8LA_OK;
+  if (!C || ldc < N) return FP8LA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(C) & 1u) != 0) return FP8LA_ERR_ALIGNMENT;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) {
+    if (!device_is_sm10x()) return FP8LA_ERR_UNSUPPORTED;
+    const int sms = sm_count();
+    zero_c_kernel_bs<<<sms > 0 ? sms * 4 : 1, 256, 0, s>>>(C, ldc, M, N);
+    return launch_status();
+  }
+  const int64_t nkb = (K + 31) / 32;
+  if (!A || !B || !sa || !sb || lda < K || ldb < K || ld_sa < nkb ||
+      ld_sb < nkb)
+    return FP8LA_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || lda % 16 != 0 || ldb % 16 != 0)
+    return FP8LA_ERR_ALIGNMENT;
+  if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) ||
+      K >= (int64_t(1) << 31) || lda >= (int64_t(1) << 39) ||
+      ldb >= (int64_t(1) << 39) || ld_sa >= (int64_t(1) << 31) ||
+      ld_sb >= (int64_t(1) << 31))
+    return FP8LA_ERR_UNSUPPORTED;
+  if (!device_is_sm10x()) return FP8LA_ERR_UNSUPPORTED;
+  CUtensorMap tmA, tmB;
+  if (!encode_2d_bs(&tmA, A, K, M, lda, BK, BM) ||
+      !encode_2d_bs(&tmB, B, K, N, ldb, BK, BN))
+    return FP8LA_ERR_CUDA;
+  unsigned *status = status_word_ptr();
+  if (!status) return FP8LA_ERR_CUDA;
+  BsArgs args{};
+  args.C = C;
+  args.ldc = ldc;
+  args.M = static_cast<int32_t>(M);
+  args.N = static_cast<int32_t>(N);
+  args.K = static_cast<int32_t>(K);
+  args.sa = sa;
+  args.ld_sa = ld_sa;
+  args.sb = sb;
+  args.ld_sb = ld_sb;
+  args.status = status;
+  args.timeout_ns = wait_timeout_ns();
+  args.c_vec16 = aligned16(C) && ldc % 8 == 0;
+  if (cudaFuncSetAttribute(gemm_e4m3_block32_kernel,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Lay::kAlloc) != cudaSuccess)
+    return FP8LA_ERR_CUDA;
+  const int sms = sm_count();
+  if (sms <= 0) return FP8LA_ERR_CUDA;
+  const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int grid = static_cast<int>(tiles < sms ? tiles : sms);
+  gemm_e4m3_block32_kernel<<<grid, kThreads, Lay::kAlloc, s>>>(tmA, tmB, args);
+  return launch_status();
 }

@@ -1,0 +1,144 @@
+"""GPU parity: 32x32 block-scaled E4M3 GEMM against the oracle, within
+
+    |C_gpu - C_ref| <= 2^-8 |C_ref| + 2^-22 K max|sa*a| max|sb*b|
+
+elementwise (C_ref the oracle's product before BF16 rounding; max|sa*a| the
+largest |tile scale x decoded code| of A, likewise for B)."""
+
+import numpy as np
+import pytest
+
+import oracle
+from _helpers import bf16_to_f64, check_pertensor, lib, random_codes, to_dev
+from precision_linear_algebra_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def _max_scaled(codes, s, rows=None):
+    """max over (m, k) of |s[m//32, k//32] * dec(codes[m, k])|."""
+    M, K = codes.shape
+    best = 0.0
+    for r0 in range(0, M, 2048):                     # bounded memory
+        blk = codes[r0:r0 + 2048]
+        d = np.abs(oracle.decode(blk))
+        st = np.abs(s[r0 // 32:(r0 + blk.shape[0] + 31) // 32].astype(np.float64))
+        sm = np.repeat(np.repeat(st, 32, axis=0), 32, axis=1)[:blk.shape[0], :K]
+        best = max(best, float((d * sm).max()))
+    return best
+
+
+def check_block(C_gpu, A, B, sa, sb, rows=None, cols=None, what="", maxes=None):
+    K = A.shape[1]
+    r, Cref = oracle.gemm_blockscaled_32x32(A, B, sa, sb, rows=rows, cols=cols)
+    ma, mb = maxes if maxes is not None else (_max_scaled(A, sa), _max_scaled(B, sb))
+    bound = oracle.bound_blockscaled_32x32(r, K, ma, mb)
+    assert np.all(np.isfinite(C_gpu)), what
+    bad = np.abs(C_gpu - r) > bound
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError("%s: %d/%d outside bound; at %s got %r want %r bound %r"
+                             % (what, bad.sum(), bad.size, i, C_gpu[i], r[i], bound[i]))
+    return float(np.mean(C_gpu == oracle.bf16_bits_to_float(Cref)))
+
+
+def _run(fl, A, B, sa, sb, ldc_pad=0):
+    import torch
+    M, K = A.shape
+    N = B.shape[0]
+    kp = max(16, (K + 15) // 16 * 16)
+    dA = torch.zeros((M, kp), dtype=torch.uint8, device="cuda")
+    dB = torch.zeros((N, kp), dtype=torch.uint8, device="cuda")
+    dA[:, :K] = to_dev(A)
+    dB[:, :K] = to_dev(B)
+    Cs = torch.full((M, N + ldc_pad), 5.0, dtype=torch.bfloat16, device="cuda")
+    C = Cs[:, :N]
+    fl.gemm_blockscaled_32x32(dA[:, :K], dB[:, :K], to_dev(sa), to_dev(sb), C=C)
+    torch.cuda.synchronize()
+    assert fl.device_status() == 0
+    if ldc_pad:
+        assert torch.all(Cs[:, N:] == 5.0)
+    return bf16_to_f64(C.contiguous())
+
+
+def _scales(rng, rows, K):
+    return rng.uniform(1e-3, 2.0, (-(-rows // 32), -(-K // 32))).astype(np.float32)
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (128, 128, 128), (128, 128, 32), (128, 128, 48), (256, 384, 512),
+    (300, 200, 100), (1, 1, 16), (640, 256, 1024), (129, 130, 272),
+])
+def test_random_codes_random_scales(M, N, K):
+    fl = lib()
+    rng = np.random.default_rng(M + 3 * N + 7 * K)
+    A, B = random_codes(rng, (M, K)), random_codes(rng, (N, K))
+    sa, sb = _scales(rng, M, K), _scales(rng, N, K)
+    got = _run(fl, A, B, sa, sb, ldc_pad=8 if N % 8 == 0 else 0)
+    frac = check_block(got, A, B, sa, sb, what="%dx%dx%d" % (M, N, K))
+    assert frac > 0.98
+
+
+def test_equal_scales_match_pertensor_bound():
+    fl = lib()
+    rng = np.random.default_rng(2)
+    M, N, K = 256, 256, 512
+    A, B = random_codes(rng, (M, K)), random_codes(rng, (N, K))
+    sa = np.full((M // 32, K // 32), 0.25, np.float32)
+    sb = np.full((N // 32, K // 32), 3.0, np.float32)
+    got = _run(fl, A, B, sa, sb)
+    check_pertensor(got, A, B, np.float32(0.25), np.float32(3.0), what="equal scales")
+
+
+def test_one_hot_k_block():
+    """Only K block 3 has nonzero scales: C is that block's product alone."""
+    fl = lib()
+    rng = np.random.default_rng(3)
+    M, N, K = 128, 128, 256
+    A, B = random_codes(rng, (M, K)), random_codes(rng, (N, K))
+    sa = np.zeros((4, 8), np.float32)
+    sb = np.ones((4, 8), np.float32)
+    sa[:, 3] = 0.5
+    got = _run(fl, A, B, sa, sb)
+    check_pertensor(got, A[:, 96:128], B[:, 96:128], np.float32(0.5), np.float32(1),
+                    what="one-hot")
+
+
+def test_k_zero_writes_zeros():
+    import torch
+    fl = lib()
+    C = torch.full((64, 64), 1.0, dtype=torch.bfloat16, device="cuda")
+    fl.fp8_gemm_blockscaled_32x32(0, 16, 0, 16, C.data_ptr(), 64, 64, 64, 0, 0, 1, 0, 1,
+                                  torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert torch.all(C == 0)
+
+
+@pytest.mark.parametrize("name", ["qkv", "attn_out", "gate_up", "down"])
+def test_transformer_linears_full_size_sampled(name):
+    """M=4096 tokens through each 70B-class linear: 32x32 block quantisation
+    of activations and weights on the GPU (checked against the oracle on
+    sampled tiles), then the block-scaled GEMM checked on sampled outputs."""
+    import torch
+    fl = lib()
+    X, W = workloads.transformer_linear(name, seed=0)
+    qx, sx = fl.quantize_blockwise_32x32(to_dev(X))
+    qw, sw = fl.quantize_blockwise_32x32(to_dev(W))
+    C = fl.gemm_blockscaled_32x32(qx, qw, sx, sw)
+    torch.cuda.synchronize()
+    assert fl.device_status() == 0
+    A, B = qx.cpu().numpy(), qw.cpu().numpy()
+    sa, sb = sx.cpu().numpy(), sw.cpu().numpy()
+    rng = np.random.default_rng(11)
+    # quantiser parity on sampled 64x64 regions
+    for (src, q, s) in ((X, A, sa), (W, B, sb)):
+        r0 = int(rng.integers(0, src.shape[0] // 32 - 1)) * 32
+        c0 = int(rng.integers(0, src.shape[1] // 32 - 1)) * 32
+        rq, rs = oracle.quantize_blockwise_32x32(src[r0:r0 + 64, c0:c0 + 64])
+        assert np.array_equal(q[r0:r0 + 64, c0:c0 + 64], rq)
+        assert np.array_equal(s[r0 // 32:r0 // 32 + 2, c0 // 32:c0 // 32 + 2], rs)
+    rows = np.sort(rng.choice(A.shape[0], 64, replace=False))
+    cols = np.sort(rng.choice(B.shape[0], 64, replace=False))
+    Cn = bf16_to_f64(C[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()])
+    check_block(Cn, A, B, sa, sb, rows=rows, cols=cols, what=name,
+                maxes=(_max_scaled(A, sa), _max_scaled(B, sb)))
