@@ -273,13 +273,13 @@ def _workload_pertensor(fl, torch, dev, sptr, ph):
                 qprofile=("quantize_pertensor_8192", QUANT_SOURCES))
 
 
-def _workload_blockscaled(fl, torch, dev, sptr, ph):
+def _workload_blockscaled(fl, torch, dev, sptr, ph, linears=("qkv", "attn_out", "gate_up", "down")):
     from precision_linear_algebra_gb300 import workloads
     items = []
     flops = 0.0
     qelems = 0
     gbytes = 0
-    for name in ("qkv", "attn_out", "gate_up", "down"):
+    for name in linears:
         X_np, W_np = workloads.transformer_linear(name, seed=0)
         M, K = X_np.shape
         N = W_np.shape[0]
@@ -314,7 +314,7 @@ def _workload_blockscaled(fl, torch, dev, sptr, ph):
                           "and weights [N][K] ~ N(0,0.02), then the block-scaled GEMM, for the "
                           "four 70B-class linears qkv (10240,8192), attn_out (8192,8192), gate_up "
                           "(57344,8192), down (8192,28672); seed 0"),
-                config={"M": 4096, "linears": "qkv,attn_out,gate_up,down",
+                config={"M": 4096, "linears": ",".join(linears),
                         "l2": "inputs 4.3 GB fp32 > 129 MB L2; no flush"},
                 inputs=[(it[3], it[10]) for it in items] + [(it[4], it[11]) for it in items],
                 outputs=[it[9] for it in items], quant_elems=qelems,
@@ -392,7 +392,10 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
     ph = _Phases(torch, stream)
-    W = WORKLOADS[args.workload](fl, torch, dev, sptr, ph)
+    if args.workload == "blockscaled" and args.linears:
+        W = _workload_blockscaled(fl, torch, dev, sptr, ph, tuple(args.linears.split(",")))
+    else:
+        W = WORKLOADS[args.workload](fl, torch, dev, sptr, ph)
     step = W["step"]
 
     for _ in range(max(3, args.warmup)):
@@ -506,7 +509,9 @@ def run_gpu(args):
             "e2e": {"value": world * W["flops"] / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms},
-            "gpu_launches": W["launches"] * args.steps,
+            "gpu_launches": W["launches"] * args.steps * (len(args.linears.split(",")) / 4.0
+                                                           if args.workload == "blockscaled"
+                                                           and args.linears else 1),
             "clocks": clocks,
         }
         if args.workload != "pertensor8192":
@@ -528,6 +533,9 @@ def main():
     ap.add_argument("--workload", default="pertensor8192", choices=sorted(WORKLOADS),
                     help="pertensor8192 is the headline line; the others measure the "
                          "block-scaled and grouped variants")
+    ap.add_argument("--linears", default="",
+                    help="blockscaled only: comma list of qkv,attn_out,gate_up,down "
+                         "(default: all four)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -204,6 +204,16 @@ FP8LA_API fp8la_status fp8la_diag_gemm_withheld_arrival(const uint8_t *A, int64_
                                               const float *scale_b,
                                               fp8la_stream_t stream);
 
+/*
+ * Choose the kernel behind fp8_gemm and fp8_grouped_gemm for calls made
+ * afterwards from this process: 0 = by problem shape (default), 1 = the
+ * single-CTA kernel (128 x 256 tiles), 2 = the CTA-pair kernel (256 x 256
+ * tiles on two SMs, tcgen05 cta_group::2).  Both compute the same result
+ * within the documented bound; this exists for testing and tuning.  Other
+ * values return FP8LA_ERR_INVALID_ARG.
+ */
+FP8LA_API fp8la_status fp8la_set_gemm_variant(int32_t variant);
+
 /* Human-readable name of a status code (static storage). */
 FP8LA_API const char *fp8la_status_string(fp8la_status status);
 

@@ -40,6 +40,7 @@ SIGNATURES = [
     ("fp8_get_device_status", _S, [_P]),
     ("fp8la_set_wait_timeout_ns", _S, [_I64]),
     ("fp8la_diag_gemm_withheld_arrival", _S, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _P]),
+    ("fp8la_set_gemm_variant", _S, [_I32]),
     ("fp8la_status_string", ctypes.c_char_p, [_S]),
     ("fp8la_version", _S, []),
 ]
@@ -126,6 +127,11 @@ def fp8la_set_wait_timeout_ns(ns):
 def fp8la_diag_gemm_withheld_arrival(A, lda, B, ldb, C, ldc, scale_a, scale_b, stream):
     return _call("fp8la_diag_gemm_withheld_arrival", A, lda, B, ldb, C, ldc,
                  scale_a, scale_b, stream)
+
+
+def fp8la_set_gemm_variant(variant):
+    """0 = by shape, 1 = single-CTA kernel, 2 = CTA-pair kernel."""
+    return _call("fp8la_set_gemm_variant", int(variant))
 
 
 def fp8la_version():

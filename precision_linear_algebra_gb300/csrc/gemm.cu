@@ -34,6 +34,8 @@
 //     the next group's rows, or TMA zeros) and not stored.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -97,17 +99,17 @@ struct TileInfo {
   int32_t group;
 };
 
-template <bool GROUPED>
+template <bool GROUPED, int TBM>
 __device__ __forceinline__ TileInfo tile_info(int t, const GemmArgs &a,
                                               int tiles_n, const int32_t *pref,
                                               const int32_t *offs_smem,
                                               int BN) {
   TileInfo ti;
   if (!GROUPED) {
-    const int tiles_m = (a.M + BM - 1) / BM;
+    const int tiles_m = (a.M + TBM - 1) / TBM;
     int mb, nb;
     tile_coords(t, tiles_m, tiles_n, mb, nb);
-    ti.row0 = mb * BM;
+    ti.row0 = mb * TBM;
     ti.row_end = a.M;
     ti.n0 = nb * BN;
     ti.group = 0;
@@ -121,15 +123,47 @@ __device__ __forceinline__ TileInfo tile_info(int t, const GemmArgs &a,
     }
     const int e = lo;
     const int m_lo = offs_smem[e], m_hi = offs_smem[e + 1];
-    const int tiles_m = (m_hi - m_lo + BM - 1) / BM;
+    const int tiles_m = (m_hi - m_lo + TBM - 1) / TBM;
     int mb, nb;
     tile_coords(t - pref[e], tiles_m, tiles_n, mb, nb);
-    ti.row0 = m_lo + mb * BM;
+    ti.row0 = m_lo + mb * TBM;
     ti.row_end = m_hi;
     ti.n0 = nb * BN;
     ti.group = e;
   }
   return ti;
+}
+
+// Epilogue of one accumulator row: 32 FP32 columns of TMEM -> x scale ->
+// BF16 (round to nearest even) -> C[row][n .. n+31], clipped at N.  Every
+// lane of the warp must call it (tcgen05.ld is warp-collective).
+__device__ __forceinline__ void store_chunk32(uint32_t taddr, bool row_ok,
+                                              uint16_t *crow, int n, int N,
+                                              float scale, bool vec16) {
+  uint32_t v[32];
+  tmem_ld32(taddr, v);
+  if (!row_ok || n >= N) return;
+  uint32_t w[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const __nv_bfloat162 h =
+        __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * j]), scale),
+                              __fmul_rn(__uint_as_float(v[2 * j + 1]), scale));
+    w[j] = *reinterpret_cast<const uint32_t *>(&h);
+  }
+  if (vec16 && n + 32 <= N) {
+    uint4 *dst = reinterpret_cast<uint4 *>(crow + n);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  } else {
+    // Fully unrolled so that w[] stays in registers.
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (n + j < N)
+        crow[n + j] = static_cast<uint16_t>((j & 1) ? (w[j >> 1] >> 16)
+                                                    : (w[j >> 1] & 0xFFFFu));
+  }
 }
 
 template <int BN, int STAGES, bool GROUPED>
@@ -214,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
         const TileInfo ti =
-            tile_info<GROUPED>(t, a, tiles_n, pref, offs_smem, BN);
+            tile_info<GROUPED, BM>(t, a, tiles_n, pref, offs_smem, BN);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns, a.status,
                          abort_flag)) {
@@ -297,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int cur_group = -1;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++local) {
       const TileInfo ti =
-          tile_info<GROUPED>(t, a, tiles_n, pref, offs_smem, BN);
+          tile_info<GROUPED, BM>(t, a, tiles_n, pref, offs_smem, BN);
       if (ti.group != cur_group) {
         scale = __fmul_rn(a.scale_a[ti.group], a.scale_b[ti.group]);
         cur_group = ti.group;
@@ -314,32 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + buf * BN;
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(taddr + c, v);
-        const int n = ti.n0 + c;
-        if (row_ok && n < a.N) {
-          uint32_t w[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const __nv_bfloat162 h = __floats2bfloat162_rn(
-                __fmul_rn(__uint_as_float(v[2 * j]), scale),
-                __fmul_rn(__uint_as_float(v[2 * j + 1]), scale));
-            w[j] = *reinterpret_cast<const uint32_t *>(&h);
-          }
-          if (a.c_vec16 && n + 32 <= a.N) {
-            uint4 *dst = reinterpret_cast<uint4 *>(crow + n);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2],
-                                  w[4 * j + 3]);
-          } else {
-            for (int j = 0; j < 32 && n + j < a.N; ++j)
-              crow[n + j] = static_cast<uint16_t>(
-                  (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu));
-          }
-        }
-      }
+      for (int c = 0; c < BN; c += 32)
+        store_chunk32(taddr + c, row_ok, crow, ti.n0 + c, a.N, scale,
+                      a.c_vec16 != 0);
       tc_fence_before();
       mbar_arrive(tempty_bar(buf));
     }
@@ -352,6 +363,243 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, L::kTmemCols);
+  }
+}
+
+// --------------------------------------------------------------------------
+// CTA-pair variant (tcgen05 cta_group::2).  A cluster of two CTAs on two SMs
+// computes a 256 x 256 tile: CTA r loads A rows row0 + 128r .. +127 and B
+// rows (= C columns) n0 + 128r .. +127 into its own shared memory (32 KB per
+// 128-wide K stage, 6 stages), and one thread of the leader CTA (rank 0)
+// issues M=256, N=256, K=32 MMAs that read both CTAs' shared memory and
+// accumulate into both CTAs' tensor memory (CTA r holds rows 128r.. of the
+// tile, all 256 columns).  Per SM this halves the B bytes moved per MMA
+// FLOP compared with the single-CTA 128 x 256 tile.  Both CTAs' TMA loads
+// complete on the leader's `full` barrier; the leader's commits are
+// multicast to both CTAs' `empty` / `tmem_full` barriers; both CTAs'
+// epilogue warps release an accumulator on the leader's `tmem_empty`.
+constexpr int P_BM = 256;   // tile rows per CTA pair
+constexpr int P_BN = 256;   // tile columns per CTA pair
+constexpr int P_STAGES = 6;
+
+struct PairSmem {
+  static constexpr int kABytes = 128 * BK;   // this CTA's half of A
+  static constexpr int kBBytes = 128 * BK;   // this CTA's half of B
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * P_BN;
+  static constexpr int kA = 0;
+  static constexpr int kB = kA + P_STAGES * kABytes;
+  static constexpr int kBar = kB + P_STAGES * kBBytes;
+  static constexpr int kNumBars = 2 * P_STAGES + 4 + 1;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kPrefix = kMisc + 16;
+  static constexpr int kEnd = kPrefix + (kMaxGroups + 1) * 4;
+  static constexpr int kAlloc = kEnd + 1024;
+};
+
+template <bool GROUPED>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_e4m3_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmB,
+                          const GemmArgs a) {
+  using L = PairSmem;
+  constexpr int STAGES = P_STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t *sbase = smem_raw + (base - raw_addr);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+
+  const uint32_t bar0 = base + L::kBar;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t final_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + L::kMisc);
+  volatile int *abort_flag =
+      reinterpret_cast<volatile int *>(sbase + L::kMisc + 4);
+  int32_t *pref = reinterpret_cast<int32_t *>(sbase + L::kPrefix);
+  __shared__ int32_t offs_smem[GROUPED ? kMaxGroups + 1 : 1];
+
+  const int tiles_n = (a.N + P_BN - 1) / P_BN;
+  const int nkb = (a.K + BK - 1) / BK;
+  const int cluster_id = blockIdx.x >> 1;
+  const int num_clusters = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 8);  // 4 epilogue warps in each CTA
+    }
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 5) {
+    tmem_alloc_pair(smem_addr(tmem_slot), L::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (GROUPED && warp == 0) {
+    for (int e = lane; e <= a.num_groups; e += 32) offs_smem[e] = a.m_offsets[e];
+    __syncwarp();
+    if (lane == 0) {
+      int acc = 0;
+      for (int e = 0; e < a.num_groups; ++e) {
+        pref[e] = acc;
+        const int me = offs_smem[e + 1] - offs_smem[e];
+        acc += (me > 0 ? (me + P_BM - 1) / P_BM : 0) * tiles_n;
+      }
+      pref[a.num_groups] = acc;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // peer barriers initialised before any remote use
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = GROUPED ? pref[a.num_groups]
+                                  : ((a.M + P_BM - 1) / P_BM) * tiles_n;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t s = 0, ph = 0, issued = 0;
+      bool ok = true;
+      for (int t = cluster_id; ok && t < total_tiles; t += num_clusters) {
+        const TileInfo ti =
+            tile_info<GROUPED, P_BM>(t, a, tiles_n, pref, offs_smem, P_BN);
+        const int arow = ti.row0 + 128 * static_cast<int>(rank);
+        const int brow = ti.n0 + 128 * static_cast<int>(rank);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns, a.status,
+                         abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t lf = mapa_shared(full_bar(s), 0);
+          if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * L::kStageBytes);
+          tma_load_2d_pair(base + L::kA + s * L::kABytes, &tmA, lf, kb * BK,
+                           arow);
+          if (GROUPED)
+            tma_load_3d_pair(base + L::kB + s * L::kBBytes, &tmB, lf, kb * BK,
+                             brow, ti.group);
+          else
+            tma_load_2d_pair(base + L::kB + s * L::kBBytes, &tmB, lf, kb * BK,
+                             brow);
+          ++issued;
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+      }
+      // The leader's full barriers count both CTAs' copies: drain them.
+      if (leader) {
+        for (uint32_t st = 0; st < STAGES; ++st) {
+          if (issued <= st) break;
+          const uint32_t arms = (issued - 1 - st) / STAGES + 1;
+          mbar_wait_drain(full_bar(st), (arms - 1) & 1u, a.timeout_ns,
+                          a.status);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------- MMA (leader CTA only)
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(P_BM, P_BN);
+      uint32_t s = 0, ph = 0, local = 0;
+      bool ok = true;
+      for (int t = cluster_id; ok && t < total_tiles;
+           t += num_clusters, ++local) {
+        const uint32_t buf = local & 1u, use = local >> 1;
+        if (!mbar_wait(tempty_bar(buf), (use & 1u) ^ 1u, a.timeout_ns,
+                       a.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * P_BN;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(full_bar(s), ph, a.timeout_ns, a.status,
+                         abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc =
+              smem_desc_k128_sw128(base + L::kA + s * L::kABytes);
+          const uint64_t bdesc =
+              smem_desc_k128_sw128(base + L::kB + s * L::kBBytes);
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k)
+            umma_f8f6f4_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc,
+                             (kb | k) != 0 ? 1u : 0u);
+          umma_commit_pair(empty_bar(s), 0x3);
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit_pair(tfull_bar(buf), 0x3);
+      }
+      umma_commit_pair(final_bar, 0x1);
+      mbar_wait_drain(final_bar, 0, a.timeout_ns, a.status);
+    }
+  } else {
+    // ----------------------------------------------- epilogue (both CTAs)
+    uint32_t local = 0;
+    float scale = 1.0f;
+    int cur_group = -1;
+    const uint32_t leader_tempty0 = mapa_shared(tempty_bar(0), 0);
+    const uint32_t leader_tempty1 = mapa_shared(tempty_bar(1), 0);
+    for (int t = cluster_id; t < total_tiles; t += num_clusters, ++local) {
+      const TileInfo ti =
+          tile_info<GROUPED, P_BM>(t, a, tiles_n, pref, offs_smem, P_BN);
+      if (ti.group != cur_group) {
+        scale = __fmul_rn(a.scale_a[ti.group], a.scale_b[ti.group]);
+        cur_group = ti.group;
+      }
+      const uint32_t buf = local & 1u, use = local >> 1;
+      const bool ready = mbar_wait(tfull_bar(buf), use & 1u, a.timeout_ns,
+                                   a.status, abort_flag);
+      if (!__all_sync(0xffffffffu, ready)) break;
+      tc_fence_after();
+      const int row = ti.row0 + 128 * static_cast<int>(rank) + warp * 32 + lane;
+      const bool row_ok = row < ti.row_end;
+      uint16_t *crow = a.C + static_cast<int64_t>(row) * a.ldc;
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + buf * P_BN;
+#pragma unroll 1
+      for (int c = 0; c < P_BN; c += 32)
+        store_chunk32(taddr + c, row_ok, crow, ti.n0 + c, a.N, scale,
+                      a.c_vec16 != 0);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader)
+          mbar_arrive(tempty_bar(buf));
+        else
+          mbar_arrive_cluster(buf ? leader_tempty1 : leader_tempty0);
+      }
+    }
+  }
+
+  // ------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // no CTA leaves while its peer may still signal it
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, L::kTmemCols);
   }
 }
 
@@ -426,6 +674,44 @@ fp8la_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB,
   return launch_status();
 }
 
+// Launch the CTA-pair kernel on clusters of two CTAs, as many clusters as
+// can be resident at once (at most one per pair tile).
+template <bool GROUPED>
+fp8la_status launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB,
+                              const GemmArgs &args, int64_t max_tiles,
+                              cudaStream_t s) {
+  using L = PairSmem;
+  auto kern = gemm_e4m3_pair_kernel<GROUPED>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           L::kAlloc) != cudaSuccess)
+    return FP8LA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(2, 1, 1);
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess ||
+      clusters < 1)
+    return FP8LA_ERR_CUDA;
+  int64_t n = max_tiles < clusters ? max_tiles : clusters;
+  if (n < 1) n = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * n), 1, 1);
+  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, args) != cudaSuccess)
+    return FP8LA_ERR_CUDA;
+  return launch_status();
+}
+
+// Kernel choice: 0 = by shape, 1 = single-CTA kernel, 2 = CTA-pair kernel.
+std::atomic<int> g_variant{0};
+
 fp8la_status check_operands(const uint8_t *A, int64_t lda, const uint8_t *B,
                             int64_t ldb, const uint16_t *C, int64_t ldc,
                             int64_t M, int64_t N, int64_t K) {
@@ -459,9 +745,14 @@ fp8la_status gemm_pertensor_impl(const uint8_t *A, int64_t lda,
     zero_c_kernel<<<sms > 0 ? sms * 4 : 1, 256, 0, s>>>(C, ldc, M, N);
     return launch_status();
   }
+  // The CTA-pair kernel (256 x 256 tiles) unless the problem has too few
+  // rows to fill a pair tile, or the caller asked otherwise; the diagnostic
+  // path always uses the single-CTA kernel.
+  const int v = g_variant.load();
+  const bool pair = !withhold && (v == 2 || (v == 0 && M > BM));
   CUtensorMap tmA, tmB;
   if (!encode_2d(&tmA, A, K, M, lda, BK, BM) ||
-      !encode_2d(&tmB, B, K, N, ldb, BK, kBN))
+      !encode_2d(&tmB, B, K, N, ldb, BK, pair ? 128 : kBN))
     return FP8LA_ERR_CUDA;
   unsigned *status = status_word_ptr();
   if (!status) return FP8LA_ERR_CUDA;
@@ -477,6 +768,10 @@ fp8la_status gemm_pertensor_impl(const uint8_t *A, int64_t lda,
   args.timeout_ns = wait_timeout_ns();
   args.withhold_first = withhold;
   args.c_vec16 = aligned16(C) && ldc % 8 == 0;
+  if (pair) {
+    const int64_t tiles = ((M + P_BM - 1) / P_BM) * ((N + P_BN - 1) / P_BN);
+    return launch_gemm_pair<false>(tmA, tmB, args, tiles, s);
+  }
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + kBN - 1) / kBN);
   return launch_gemm<false>(tmA, tmB, args, tiles, s);
 }
@@ -528,9 +823,13 @@ extern "C" fp8la_status fp8_grouped_gemm(
   if (b_group_stride % 16 != 0 || b_group_stride < N * ldb)
     return b_group_stride % 16 != 0 ? FP8LA_ERR_ALIGNMENT
                                     : FP8LA_ERR_INVALID_ARG;
+  // CTA pairs when groups average at least one pair tile of rows.
+  const int v = g_variant.load();
+  const bool pair = v == 2 || (v == 0 && m_capacity >= int64_t(P_BM) * num_groups);
   CUtensorMap tmA, tmB;
   if (!encode_2d(&tmA, A, K, m_capacity, lda, BK, BM) ||
-      !encode_3d(&tmB, B, K, N, num_groups, ldb, b_group_stride, BK, kBN))
+      !encode_3d(&tmB, B, K, N, num_groups, ldb, b_group_stride, BK,
+                 pair ? 128 : kBN))
     return FP8LA_ERR_CUDA;
   unsigned *status = status_word_ptr();
   if (!status) return FP8LA_ERR_CUDA;
@@ -549,7 +848,18 @@ extern "C" fp8la_status fp8_grouped_gemm(
   args.timeout_ns = wait_timeout_ns();
   // Upper bound on the tile count without reading m_offsets: each group
   // adds at most one partial row block.
+  if (pair) {
+    const int64_t tiles = ((m_capacity + P_BM - 1) / P_BM + num_groups) *
+                          ((N + P_BN - 1) / P_BN);
+    return launch_gemm_pair<true>(tmA, tmB, args, tiles, s);
+  }
   const int64_t tiles =
       ((m_capacity + BM - 1) / BM + num_groups) * ((N + kBN - 1) / kBN);
   return launch_gemm<true>(tmA, tmB, args, tiles, s);
+}
+
+extern "C" fp8la_status fp8la_set_gemm_variant(int32_t variant) {
+  if (variant < 0 || variant > 2) return FP8LA_ERR_INVALID_ARG;
+  g_variant.store(variant);
+  return FP8LA_OK;
 }

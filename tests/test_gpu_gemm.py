@@ -15,6 +15,15 @@ from precision_linear_algebra_gb300 import workloads
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=[1, 2], ids=["single_cta", "cta_pair"])
+def variant(request):
+    """Run a test once per GEMM kernel (single-CTA and CTA-pair)."""
+    fl = lib()
+    fl.fp8la_set_gemm_variant(request.param)
+    yield request.param
+    fl.fp8la_set_gemm_variant(0)
+
+
 def _gemm(fl, A, B, sa, sb, ldc_pad=0):
     import torch
     M, K = A.shape
@@ -51,7 +60,7 @@ def _gemm(fl, A, B, sa, sb, ldc_pad=0):
     (129, 257, 144),
     (640, 1280, 384),
 ])
-def test_random_codes(M, N, K):
+def test_random_codes(M, N, K, variant):
     fl = lib()
     rng = np.random.default_rng(M * 7 + N * 13 + K)
     A, B = random_codes(rng, (M, K)), random_codes(rng, (N, K))
@@ -61,7 +70,7 @@ def test_random_codes(M, N, K):
     assert frac > 0.99
 
 
-def test_identity_operand_selects_columns():
+def test_identity_operand_selects_columns(variant):
     """A = I (code 0x38 = 1): C = dec(B)^T exactly (every E4M3 value is a bf16)."""
     fl = lib()
     rng = np.random.default_rng(3)
@@ -72,7 +81,7 @@ def test_identity_operand_selects_columns():
     assert np.array_equal(got, oracle.decode(B).T)
 
 
-def test_one_hot_rows_and_ldc_padding():
+def test_one_hot_rows_and_ldc_padding(variant):
     fl = lib()
     rng = np.random.default_rng(4)
     M, N, K = 200, 300, 256
@@ -91,7 +100,7 @@ def test_k_zero_writes_zeros():
     assert got.shape == (5, 9) and np.all(got == 0)
 
 
-def test_saturated_operands():
+def test_saturated_operands(variant):
     fl = lib()
     M, N, K = 128, 256, 512
     A = np.full((M, K), 0x7E, np.uint8)
@@ -101,7 +110,7 @@ def test_saturated_operands():
 
 
 @pytest.mark.parametrize("n", [256, 1024])
-def test_square_configs_end_to_end(n):
+def test_square_configs_end_to_end(n, variant):
     """Quantise N(0,1) operands on the GPU, then GEMM; check both steps."""
     import torch
     fl = lib()
@@ -118,7 +127,7 @@ def test_square_configs_end_to_end(n):
     assert frac > 0.99
 
 
-def test_8192_outliers_sampled():
+def test_8192_outliers_sampled(variant):
     """Full-size 8192^3 with outliers, in the launch configuration the
     benchmark times; the oracle checks 96 sampled rows x all columns plus
     all rows x 64 sampled columns."""

@@ -12,6 +12,14 @@ from precision_linear_algebra_gb300 import workloads
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=[1, 2], ids=["single_cta", "cta_pair"])
+def variant(request):
+    fl = lib()
+    fl.fp8la_set_gemm_variant(request.param)
+    yield request.param
+    fl.fp8la_set_gemm_variant(0)
+
+
 def _grouped(fl, A, offs, B, sa, sb, cap_extra=0):
     import torch
     cap = A.shape[0] + cap_extra
@@ -41,7 +49,7 @@ def _grouped(fl, A, offs, B, sa, sb, cap_extra=0):
     ([1000], 600, 200),
     ([5, 17, 250, 3, 0, 0, 140, 77], 272, 160),
 ])
-def test_grouped_random_codes(counts, N, K):
+def test_grouped_random_codes(counts, N, K, variant):
     fl = lib()
     rng = np.random.default_rng(sum(counts) + N + K)
     offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
@@ -58,7 +66,7 @@ def test_grouped_random_codes(counts, N, K):
     assert np.all(got[offs[-1]:] == 3.0), "rows past the last group were written"
 
 
-def test_grouped_equals_per_group_gemm_calls():
+def test_grouped_equals_per_group_gemm_calls(variant):
     """One grouped launch equals E separate fp8_gemm calls, bit for bit."""
     import torch
     fl = lib()
@@ -80,7 +88,7 @@ def test_grouped_equals_per_group_gemm_calls():
         assert np.array_equal(bf16_to_f64(C), got[lo:hi])
 
 
-def test_moe_layer_full_size_sampled():
+def test_moe_layer_full_size_sampled(variant):
     """8 experts, K 4096, N 14336, 16384 routed rows with Dirichlet counts;
     per-expert per-tensor quantisation on the GPU, one grouped launch; the
     oracle checks sampled rows of every group against sampled columns."""
