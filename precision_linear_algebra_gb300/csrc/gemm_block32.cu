@@ -15,21 +15,23 @@
 // by one tcgen05.mma (M=128, N=128, K=32) into a fresh TMEM buffer and then
 // weighted and added on the CUDA cores.
 //
-// Design (one CTA per SM, persistent, 10 warps):
-//   * warp 8: producer.  Lane 0 issues the TMA loads of a 128 x 128 A tile
+// Design (one CTA per SM, persistent, 18 warps):
+//   * warp 16: producer.  Lane 0 issues the TMA loads of a 128 x 128 A tile
 //     and a 128 x 128 B tile per 128-wide K stage (6-stage ring); all 32
 //     lanes fetch the stage's 16 A-tile and 16 B-tile scales (4 row tiles x
 //     4 K blocks each) into shared memory beside it.
-//   * warp 9: MMA issuer (lane 0).  One MMA per 32-wide K block into one of
+//   * warp 17: MMA issuer (lane 0).  One MMA per 32-wide K block into one of
 //     four 128-column TMEM partial buffers (`pfull` / `pempty` ring).
-//   * warps 0-7: promotion.  Warp w reads TMEM lanes 32(w%4).. (C rows) and
-//     columns 64(w/4)..+63; each thread keeps its row's 64 FP32
-//     accumulators in registers and, for every K block, adds
-//     (sa*sb) * partial with packed FP32 FMAs (fma.rn.f32x2).  The scale is
-//     uniform over a warp's 32 x 32 chunk.  After the last K block it
-//     rounds to BF16 and stores.
-//   * A stage is recycled only when its MMAs have completed and all eight
-//     promotion warps have read its scales (empty barrier count 1 + 8).
+//   * warps 0-15: promotion, four per SM sub-partition.  Warp w reads TMEM
+//     lanes 32(w%4).. (C rows) and columns 32(w/4)..+31, exactly one 32 x 32
+//     scale tile, so its scale sa*sb is one number per K block.  Each thread
+//     keeps its row's 32 FP32 accumulators in registers and, for every K
+//     block, adds (sa*sb) * partial with packed FP32 FMAs (fma.rn.f32x2).
+//     Each partial buffer is released as soon as it has reached registers;
+//     the four warps of a sub-partition hide each other's TMEM-load latency.
+//     After the last K block the thread rounds to BF16 and stores 64 bytes.
+//   * A stage is recycled only when its MMAs have completed and all sixteen
+//     promotion warps have read its scales (empty barrier count 1 + 16).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -44,12 +46,18 @@ constexpr int BK = 128;          // K per stage (bytes = E4M3 values)
 constexpr int KB = 32;           // scale block along K, = K per MMA
 constexpr int STAGES = 6;
 constexpr int NPART = 4;         // TMEM partial buffers of BN columns
-constexpr int kPromoWarps = 8;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kPromoWarps = 16;
+constexpr int kProducerWarp = 16;
+constexpr int kMmaWarp = 17;
+constexpr int kThreads = 576;
 constexpr int GROUP_M = 16;
 constexpr int kTmemCols = NPART * BN;  // 512
+
+// Promotion arithmetic: 1 = packed fma.rn.f32x2 (two FMAs per instruction),
+// 0 = scalar fma.rn.f32.  Both round each FMA once.
+#ifndef FP8LA_BS_PACKED_FMA
+#define FP8LA_BS_PACKED_FMA 1
+#endif
 
 struct BsArgs {
   uint16_t *C;
@@ -248,18 +256,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ----------------------------------------------------------- promotion
     const int q = warp & 3;          // TMEM lane quarter = 32-row tile
-    const int h = warp >> 2;         // column half: 64h .. 64h + 63
+    const int c = warp >> 2;         // 32-column slice = column tile
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     uint32_t s = 0, ph = 0, p = 0, pph = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
       int mb, nb;
       tile_coords(t, tiles_m, tiles_n, mb, nb);
-      uint64_t acc[32];
+      uint64_t acc[16];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) acc[j] = 0;
+      for (int j = 0; j < 16; ++j) acc[j] = 0;
       for (int ks = 0; ok && ks < nks; ++ks) {
-        // Acquire the producer's scale writes for this stage.
+        // This stage's four scale products, then release the stage's
+        // scale slots (the MMA commit releases its operand tiles).
         const bool sready = mbar_wait(full_bar(s), ph, a.timeout_ns,
                                       a.status, abort_flag);
         if (!__all_sync(0xffffffffu, sready)) {
@@ -267,11 +276,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const float *sc = scales + s * 32;
-#pragma unroll 1
-        for (int k = 0; k < BK / KB; ++k) {
-          const float sav = sc[k * 4 + q];
-          const float s0 = __fmul_rn(sav, sc[16 + k * 4 + 2 * h]);
-          const float s1 = __fmul_rn(sav, sc[16 + k * 4 + 2 * h + 1]);
+        float s4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          s4[k] = __fmul_rn(sc[k * 4 + q], sc[16 + k * 4 + c]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(s));
+        if (++s == STAGES) { s = 0; ph ^= 1u; }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
           const bool pready = mbar_wait(pfull_bar(p), pph, a.timeout_ns,
                                         a.status, abort_flag);
           if (!__all_sync(0xffffffffu, pready)) {
@@ -279,54 +292,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t taddr = tmem_base + lane_base + p * BN + 64 * h;
           uint32_t r[32];
-          tmem_ld32(taddr, r);
-          const uint64_t s0x2 = pack2(s0, s0);
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            fma2(acc[j], s0x2, pack2(__uint_as_float(r[2 * j]),
-                                     __uint_as_float(r[2 * j + 1])));
-          tmem_ld32(taddr + 32, r);
-          const uint64_t s1x2 = pack2(s1, s1);
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            fma2(acc[16 + j], s1x2, pack2(__uint_as_float(r[2 * j]),
-                                          __uint_as_float(r[2 * j + 1])));
+          tmem_ld32(tmem_base + lane_base + p * BN + 32 * c, r);
+          // The partial is in registers: hand its buffer back to the MMA.
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(pempty_bar(p));
           if (++p == NPART) { p = 0; pph ^= 1u; }
+#if FP8LA_BS_PACKED_FMA
+          const uint64_t s2 = pack2(s4[k], s4[k]);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            fma2(acc[j], s2, pack2(__uint_as_float(r[2 * j]),
+                                   __uint_as_float(r[2 * j + 1])));
+#else
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float lo, hi;
+            unpack2(acc[j], lo, hi);
+            lo = __fmaf_rn(s4[k], __uint_as_float(r[2 * j]), lo);
+            hi = __fmaf_rn(s4[k], __uint_as_float(r[2 * j + 1]), hi);
+            acc[j] = pack2(lo, hi);
+          }
+#endif
         }
-        if (!ok) break;
-        // This warp is done with the stage's scales.
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(s));
-        if (++s == STAGES) { s = 0; ph ^= 1u; }
       }
       if (!ok) break;
-      // Epilogue: round to BF16 and store this thread's 64 columns.
+      // Epilogue: round to BF16 and store this thread's 32 columns.
       const int row = mb * BM + q * 32 + lane;
-      const int n = nb * BN + 64 * h;
+      const int n = nb * BN + 32 * c;
       if (row < a.M && n < a.N) {
         uint16_t *crow = a.C + static_cast<int64_t>(row) * a.ldc;
-        uint32_t w[32];
+        uint32_t w[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < 16; ++j) {
           float lo, hi;
           unpack2(acc[j], lo, hi);
           const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
           w[j] = *reinterpret_cast<const uint32_t *>(&b2);
         }
-        if (a.c_vec16 && n + 64 <= a.N) {
+        if (a.c_vec16 && n + 32 <= a.N) {
           uint4 *dst = reinterpret_cast<uint4 *>(crow + n);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
+          for (int j = 0; j < 4; ++j)
             dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2],
                                 w[4 * j + 3]);
         } else {
 #pragma unroll
-          for (int j = 0; j < 64; ++j)
+          for (int j = 0; j < 32; ++j)
             if (n + j < a.N)
               crow[n + j] = static_cast<uint16_t>(
                   (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu));

@@ -12,7 +12,8 @@
 // a 128-bit-load grid reduction whose blocks combine their maxima with one
 // atomicMax on the float's bit pattern (non-negative floats order like
 // their unsigned bit patterns; max is exact, so the result does not depend
-// on the order), then a cast pass.  The block quantiser needs one pass: a
+// on the order), then a cast pass that walks the tensor backwards so that
+// it starts on the part the reduction left in L2.  The block quantiser needs one pass: a
 // 32x32 fp32 tile (4 KB) fits one warp's registers.
 #include <cuda_fp8.h>
 
@@ -146,19 +147,22 @@ __global__ void __launch_bounds__(kThreads)
   int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (VEC == 4) {
     if (contiguous) {
+      // Walk the tensor from its end: the amax pass has just streamed it
+      // front to back, so its tail is still in L2.  Unit u = n - 1 - i.
       const float4 *x4 = reinterpret_cast<const float4 *>(x);
       uint32_t *q4 = reinterpret_cast<uint32_t *>(q);
+      const int64_t last = n - 1;
       for (; i + 3 * stride < n; i += 4 * stride) {
-        const float4 a = ld_stream4(x4 + i);
-        const float4 b = ld_stream4(x4 + i + stride);
-        const float4 c = ld_stream4(x4 + i + 2 * stride);
-        const float4 d = ld_stream4(x4 + i + 3 * stride);
-        q4[i] = cvt4(a, qs);
-        q4[i + stride] = cvt4(b, qs);
-        q4[i + 2 * stride] = cvt4(c, qs);
-        q4[i + 3 * stride] = cvt4(d, qs);
+        const float4 a = ld_stream4(x4 + (last - i));
+        const float4 b = ld_stream4(x4 + (last - i - stride));
+        const float4 c = ld_stream4(x4 + (last - i - 2 * stride));
+        const float4 d = ld_stream4(x4 + (last - i - 3 * stride));
+        q4[last - i] = cvt4(a, qs);
+        q4[last - i - stride] = cvt4(b, qs);
+        q4[last - i - 2 * stride] = cvt4(c, qs);
+        q4[last - i - 3 * stride] = cvt4(d, qs);
       }
-      for (; i < n; i += stride) q4[i] = cvt4(ld_stream4(x4 + i), qs);
+      for (; i < n; i += stride) q4[last - i] = cvt4(ld_stream4(x4 + (last - i)), qs);
     } else {
       for (; i < n; i += stride) {
         const int64_t r = i / upr, c = i - r * upr;
