@@ -47,6 +47,20 @@ def _dist_env():
         int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(x, device=None):
+    """max of a per-rank float over all ranks (identity when not distributed).
+
+    The only collective of the replica benchmark: each rank times its own
+    replica and the job's time is the slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -268,7 +282,7 @@ def _workload_pertensor(fl, torch, dev, sptr, ph):
                 config={"M": N_SIZE, "N": N_SIZE, "K": N_SIZE,
                         "l2": "inputs 2 x 268 MB fp32 > 129 MB L2; no flush"},
                 inputs=[(A, A_np), (B, B_np)], outputs=[C],
-                quant_elems=2 * N_SIZE * N_SIZE, gemm_label="gemm_e4m3_kernel<256,4,false>",
+                quant_elems=2 * N_SIZE * N_SIZE, gemm_label="gemm_e4m3_pair_kernel<false>",
                 gemm_bytes=GEMM_BYTES, profile=("gemm_e4m3_pertensor_8192", GEMM_SOURCES),
                 qprofile=("quantize_pertensor_8192", QUANT_SOURCES))
 
@@ -363,7 +377,7 @@ def _workload_grouped(fl, torch, dev, sptr, ph):
                 config={"experts": E, "N": N, "K": K, "rows": Mt,
                         "l2": "inputs 2.1 GB fp32 > 129 MB L2; no flush"},
                 inputs=[(X, X_np), (W, W_np)], outputs=[C], quant_elems=Mt * K + E * N * K,
-                gemm_label="gemm_e4m3_kernel<256,4,true>",
+                gemm_label="gemm_e4m3_pair_kernel<true>",
                 gemm_bytes=Mt * K + E * N * K + 2 * Mt * N,
                 profile=("gemm_e4m3_grouped_moe", GEMM_SOURCES),
                 qprofile=("quantize_pertensor_8192", QUANT_SOURCES))
@@ -436,9 +450,7 @@ def run_gpu(args):
     if fl.fp8_get_device_status(sptr) != 0:
         raise RuntimeError("device status reports a timeout in the timed region")
     if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = tt.item()
+        ms_total = max_over_ranks(ms_total, dev)
     ms_step = ms_total / args.steps
     value = world * W["flops"] / (ms_step * 1e-3) / 1e12
 
@@ -467,9 +479,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = tt.item()
+        e2e_ms = max_over_ranks(e2e_ms, dev)
     h2d = sum(h.numel() * h.element_size() for _, h in hosts)
     d2h = sum(h.numel() * h.element_size() for _, h in outs)
 

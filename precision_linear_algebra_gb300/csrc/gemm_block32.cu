@@ -15,23 +15,30 @@
 // by one tcgen05.mma (M=128, N=128, K=32) into a fresh TMEM buffer and then
 // weighted and added on the CUDA cores.
 //
-// Design (one CTA per SM, persistent, 18 warps):
-//   * warp 16: producer.  Lane 0 issues the TMA loads of a 128 x 128 A tile
-//     and a 128 x 128 B tile per 128-wide K stage (6-stage ring); all 32
-//     lanes fetch the stage's 16 A-tile and 16 B-tile scales (4 row tiles x
-//     4 K blocks each) into shared memory beside it.
-//   * warp 17: MMA issuer (lane 0).  One MMA per 32-wide K block into one of
-//     four 128-column TMEM partial buffers (`pfull` / `pempty` ring).
-//   * warps 0-15: promotion, four per SM sub-partition.  Warp w reads TMEM
-//     lanes 32(w%4).. (C rows) and columns 32(w/4)..+31, exactly one 32 x 32
-//     scale tile, so its scale sa*sb is one number per K block.  Each thread
-//     keeps its row's 32 FP32 accumulators in registers and, for every K
-//     block, adds (sa*sb) * partial with packed FP32 FMAs (fma.rn.f32x2).
-//     Each partial buffer is released as soon as it has reached registers;
-//     the four warps of a sub-partition hide each other's TMEM-load latency.
-//     After the last K block the thread rounds to BF16 and stores 64 bytes.
-//   * A stage is recycled only when its MMAs have completed and all sixteen
-//     promotion warps have read its scales (empty barrier count 1 + 16).
+// Design (one CTA per SM, persistent, 10 warps).  The promotion costs one
+// FP32 FMA per output per 32-wide K block, against 32 tensor-core FMAs: on
+// 128 FP32 lanes per SM versus 8192 tensor FMAs per clock this caps the
+// kernel near half the dense FP8 peak, so the design keeps the FMA pipe
+// busy and puts all synchronisation at the granularity of 128-wide K stages:
+//   * warp 8: producer.  Lane 0 issues the TMA loads of a 128 x 128 A tile
+//     and a 64 x 128 B tile per 128-wide K stage (8-stage ring); all 32 lanes
+//     compute the stage's 32 scale products sa[row tile][kb] * sb[col
+//     tile][kb] (4 row tiles x 2 column tiles x 4 K blocks) into shared
+//     memory beside it.
+//   * warp 9: MMA issuer (lane 0).  Per stage, four MMAs (M=128, N=64, K=32,
+//     one per 32-wide K block) into the four 64-column TMEM partial buffers
+//     of one of two buffer sets; one commit hands the whole set over.
+//   * warps 0-7: promotion.  Warp w reads TMEM lanes 32(w%4).. (C rows) and
+//     columns 32(w/4)..+31 of each partial, exactly one 32 x 32 scale tile,
+//     so its scale is one number per K block (read as one 16-byte vector per
+//     stage).  Each thread keeps its row's 32 FP32 accumulators in
+//     registers and adds (sa*sb) * partial with FP32 FMAs, two K blocks'
+//     partials loaded per TMEM wait.  After the last stage of a tile it
+//     rounds to BF16 and stores 64 bytes.
+//   * A stage is recycled only when its MMAs have completed and all eight
+//     promotion warps have read its scale products (empty count 1 + 8); a
+//     partial-buffer set is reused once all eight warps hold its data in
+//     registers (pempty count 8).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -41,23 +48,18 @@ namespace fp8la {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 128;
+constexpr int BN = 64;
 constexpr int BK = 128;          // K per stage (bytes = E4M3 values)
 constexpr int KB = 32;           // scale block along K, = K per MMA
-constexpr int STAGES = 6;
-constexpr int NPART = 4;         // TMEM partial buffers of BN columns
-constexpr int kPromoWarps = 16;
-constexpr int kProducerWarp = 16;
-constexpr int kMmaWarp = 17;
-constexpr int kThreads = 576;
+constexpr int KPS = BK / KB;     // K blocks per stage (4)
+constexpr int STAGES = 8;
+constexpr int NSETS = 2;         // TMEM partial-buffer sets, KPS buffers each
+constexpr int kPromoWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
 constexpr int GROUP_M = 16;
-constexpr int kTmemCols = NPART * BN;  // 512
-
-// Promotion arithmetic: 1 = packed fma.rn.f32x2 (two FMAs per instruction),
-// 0 = scalar fma.rn.f32.  Both round each FMA once.
-#ifndef FP8LA_BS_PACKED_FMA
-#define FP8LA_BS_PACKED_FMA 1
-#endif
+constexpr int kTmemCols = NSETS * KPS * BN;  // 512
 
 struct BsArgs {
   uint16_t *C;
@@ -80,7 +82,7 @@ struct Lay {
   static constexpr int kB = kA + STAGES * kABytes;
   static constexpr int kScale = kB + STAGES * kBBytes;     // STAGES x 32 floats
   static constexpr int kBar = kScale + STAGES * 32 * 4;
-  static constexpr int kNumBars = 2 * STAGES + 2 * NPART + 1;
+  static constexpr int kNumBars = 2 * STAGES + 2 * NSETS + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kEnd = kMisc + 16;
   static constexpr int kAlloc = kEnd + 1024;
@@ -95,21 +97,6 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n,
   const int r = t - g * per_group;
   mb = first_m + r % gm;
   nb = r / gm;
-}
-
-__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-
-__device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-
-// acc = s * p + acc, two lanes at once, each rounded once.
-__device__ __forceinline__ void fma2(uint64_t &acc, uint64_t s, uint64_t p) {
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(s), "l"(p));
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -128,8 +115,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
   auto pfull_bar = [&](int p) { return bar0 + 8u * (2 * STAGES + p); };
-  auto pempty_bar = [&](int p) { return bar0 + 8u * (2 * STAGES + NPART + p); };
-  const uint32_t final_bar = bar0 + 8u * (2 * STAGES + 2 * NPART);
+  auto pempty_bar = [&](int p) { return bar0 + 8u * (2 * STAGES + NSETS + p); };
+  const uint32_t final_bar = bar0 + 8u * (2 * STAGES + 2 * NSETS);
   float *scales = reinterpret_cast<float *>(sbase + Lay::kScale);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + Lay::kMisc);
   volatile int *abort_flag =
@@ -147,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1 + kPromoWarps);
     }
-    for (int p = 0; p < NPART; ++p) {
+    for (int p = 0; p < NSETS; ++p) {
       mbar_init(pfull_bar(p), 1);
       mbar_init(pempty_bar(p), kPromoWarps);
     }
@@ -183,19 +170,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        // Lane l < 16: sa of row tile m0/32 + (l & 3), K block 4ks + (l >> 2);
-        // lane l >= 16: the same for sb and column tiles.
-        const int i = lane & 3, j = (lane >> 2) & 3;
-        const int kb = ks * 4 + j;
+        // Lane l: K block kb = 4ks + (l & 3) of scale tile
+        // (row tile q, column tile c) = ((l >> 3) & 3 ... ) laid out as
+        // scales[s][(q * 2 + c) * 4 + (kb & 3)], so that promotion warp
+        // (q, c) reads its stage's four products as one 16-byte vector.
+        const int k4 = lane & 3, c = (lane >> 2) & 1, q = lane >> 3;
+        const int kb = ks * KPS + k4;
+        const int rt = m0 / 32 + q, ct = n0 / 32 + c;
         float v = 0.0f;
-        if (lane < 16) {
-          const int rt = m0 / 32 + i;
-          if (rt < srow_a && kb < nkb) v = a.sa[rt * a.ld_sa + kb];
-        } else {
-          const int ct = n0 / 32 + i;
-          if (ct < srow_b && kb < nkb) v = a.sb[ct * a.ld_sb + kb];
-        }
-        scales[s * 32 + lane] = v;
+        if (rt < srow_a && ct < srow_b && kb < nkb)
+          v = __fmul_rn(a.sa[rt * a.ld_sa + kb], a.sb[ct * a.ld_sb + kb]);
+        scales[s * 32 + (q * 2 + c) * 4 + k4] = v;
         __syncwarp();
         if (lane == 0) {
           mbar_arrive_expect_tx(full_bar(s), Lay::kStageBytes);
@@ -219,11 +204,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
-      uint32_t s = 0, ph = 0, p = 0, pph = 0;
+      uint32_t s = 0, ph = 0, set = 0, sph = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
         for (int ks = 0; ok && ks < nks; ++ks) {
           if (!mbar_wait(full_bar(s), ph, a.timeout_ns, a.status,
+                         abort_flag) ||
+              !mbar_wait(pempty_bar(set), sph ^ 1u, a.timeout_ns, a.status,
                          abort_flag)) {
             ok = false;
             break;
@@ -233,20 +220,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               smem_desc_k128_sw128(base + Lay::kA + s * Lay::kABytes);
           const uint64_t bdesc =
               smem_desc_k128_sw128(base + Lay::kB + s * Lay::kBBytes);
-          for (int k = 0; k < BK / KB; ++k) {
-            if (!mbar_wait(pempty_bar(p), pph ^ 1u, a.timeout_ns, a.status,
-                           abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            umma_f8f6f4(tmem_base + p * BN, adesc + 2u * k, bdesc + 2u * k,
-                        idesc, 0u);
-            umma_commit(pfull_bar(p));
-            if (++p == NPART) { p = 0; pph ^= 1u; }
-          }
-          if (!ok) break;
+#pragma unroll
+          for (int k = 0; k < KPS; ++k)
+            umma_f8f6f4(tmem_base + (set * KPS + k) * BN, adesc + 2u * k,
+                        bdesc + 2u * k, idesc, 0u);
+          umma_commit(pfull_bar(set));
           umma_commit(empty_bar(s));
+          if (++set == NSETS) { set = 0; sph ^= 1u; }
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
       }
@@ -257,64 +237,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------------- promotion
     const int q = warp & 3;          // TMEM lane quarter = 32-row tile
     const int c = warp >> 2;         // 32-column slice = column tile
-    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    uint32_t s = 0, ph = 0, p = 0, pph = 0;
+    const uint32_t col0 = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                          32 * c;
+    uint32_t s = 0, ph = 0, set = 0, sph = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
       int mb, nb;
       tile_coords(t, tiles_m, tiles_n, mb, nb);
-      uint64_t acc[16];
+      float acc[32];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) acc[j] = 0;
+      for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
       for (int ks = 0; ok && ks < nks; ++ks) {
-        // This stage's four scale products, then release the stage's
-        // scale slots (the MMA commit releases its operand tiles).
+        // Scale products of this stage (acquired through the stage's full
+        // barrier), then let the stage go as far as this warp is concerned.
         const bool sready = mbar_wait(full_bar(s), ph, a.timeout_ns,
                                       a.status, abort_flag);
-        if (!__all_sync(0xffffffffu, sready)) {
+        const bool pready = sready &&
+                            mbar_wait(pfull_bar(set), sph, a.timeout_ns,
+                                      a.status, abort_flag);
+        if (!__all_sync(0xffffffffu, sready && pready)) {
           ok = false;
           break;
         }
-        const float *sc = scales + s * 32;
-        float s4[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          s4[k] = __fmul_rn(sc[k * 4 + q], sc[16 + k * 4 + c]);
+        const float4 sc = *reinterpret_cast<const float4 *>(
+            scales + s * 32 + (q * 2 + c) * 4);
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(s));
         if (++s == STAGES) { s = 0; ph ^= 1u; }
+        tc_fence_after();
+        const uint32_t pbase = col0 + set * KPS * BN;
+        uint32_t r0[32], r1[32];
+        // K blocks 0 and 1 of the stage.
+        tmem_ld32_async(pbase, r0);
+        tmem_ld32_async(pbase + BN, r1);
+        tmem_ld_wait32(r0);
+        tmem_ld_wait32(r1);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const bool pready = mbar_wait(pfull_bar(p), pph, a.timeout_ns,
-                                        a.status, abort_flag);
-          if (!__all_sync(0xffffffffu, pready)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          uint32_t r[32];
-          tmem_ld32(tmem_base + lane_base + p * BN + 32 * c, r);
-          // The partial is in registers: hand its buffer back to the MMA.
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(pempty_bar(p));
-          if (++p == NPART) { p = 0; pph ^= 1u; }
-#if FP8LA_BS_PACKED_FMA
-          const uint64_t s2 = pack2(s4[k], s4[k]);
+        for (int j = 0; j < 32; ++j) {
+          acc[j] = __fmaf_rn(sc.x, __uint_as_float(r0[j]), acc[j]);
+          acc[j] = __fmaf_rn(sc.y, __uint_as_float(r1[j]), acc[j]);
+        }
+        // K blocks 2 and 3; then the whole set is in registers.
+        tmem_ld32_async(pbase + 2 * BN, r0);
+        tmem_ld32_async(pbase + 3 * BN, r1);
+        tmem_ld_wait32(r0);
+        tmem_ld_wait32(r1);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pempty_bar(set));
+        if (++set == NSETS) { set = 0; sph ^= 1u; }
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            fma2(acc[j], s2, pack2(__uint_as_float(r[2 * j]),
-                                   __uint_as_float(r[2 * j + 1])));
-#else
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float lo, hi;
-            unpack2(acc[j], lo, hi);
-            lo = __fmaf_rn(s4[k], __uint_as_float(r[2 * j]), lo);
-            hi = __fmaf_rn(s4[k], __uint_as_float(r[2 * j + 1]), hi);
-            acc[j] = pack2(lo, hi);
-          }
-#endif
+        for (int j = 0; j < 32; ++j) {
+          acc[j] = __fmaf_rn(sc.z, __uint_as_float(r0[j]), acc[j]);
+          acc[j] = __fmaf_rn(sc.w, __uint_as_float(r1[j]), acc[j]);
         }
       }
       if (!ok) break;
@@ -326,9 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t w[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          float lo, hi;
-          unpack2(acc[j], lo, hi);
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
           w[j] = *reinterpret_cast<const uint32_t *>(&b2);
         }
         if (a.c_vec16 && n + 32 <= a.N) {
