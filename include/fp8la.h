@@ -138,7 +138,9 @@ FP8LA_API fp8la_status fp8_gemm(const uint8_t *A, int64_t lda, const uint8_t *B,
  * Each 32-wide K block's partial sum is formed on the tensor cores and then
  * promoted, multiplied by its tile-scale product, into an FP32 accumulator
  * on the CUDA cores.  sa: fp32 [ceil(M/32)][ld_sa], ld_sa >= ceil(K/32);
- * sb: fp32 [ceil(N/32)][ld_sb], ld_sb >= ceil(K/32).  All device.
+ * sb: fp32 [ceil(N/32)][ld_sb], ld_sb >= ceil(K/32).  All device.  The
+ * scale grids are read by TMA: sa and sb must be 16-byte aligned and ld_sa,
+ * ld_sb multiples of 4 (otherwise FP8LA_ERR_ALIGNMENT).
  */
 FP8LA_API fp8la_status fp8_gemm_blockscaled_32x32(const uint8_t *A, int64_t lda,
                                         const uint8_t *B, int64_t ldb,

@@ -174,8 +174,11 @@ def quantize_blockwise_32x32(x, q=None, scales=None):
     if q is None:
         q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
     if scales is None:
-        scales = torch.empty(((rows + 31) // 32, (cols + 31) // 32),
-                             dtype=torch.float32, device=x.device)
+        # leading dimension rounded up to 4 floats, as the block-scaled GEMM
+        # reads scale grids with TMA (16-byte rows)
+        tc = (cols + 31) // 32
+        scales = torch.empty(((rows + 31) // 32, (tc + 3) // 4 * 4),
+                             dtype=torch.float32, device=x.device)[:, :tc]
     fp8_quantize_blockwise_32x32(_ptr(x), rows, cols, x.stride(0), _ptr(q), q.stride(0),
                                  _ptr(scales), scales.stride(0), _stream())
     return q, scales

@@ -20,23 +20,23 @@
 // 128 FP32 lanes per SM versus 8192 tensor FMAs per clock this caps the
 // kernel near half the dense FP8 peak, so the design keeps the FMA pipe
 // busy and puts all synchronisation at the granularity of 128-wide K stages:
-//   * warp 8: producer.  Lane 0 issues the TMA loads of a 128 x 128 A tile
-//     and a 64 x 128 B tile per 128-wide K stage (8-stage ring); all 32 lanes
-//     compute the stage's 32 scale products sa[row tile][kb] * sb[col
-//     tile][kb] (4 row tiles x 2 column tiles x 4 K blocks) into shared
-//     memory beside it.
+//   * warp 8: producer (lane 0).  Per 128-wide K stage (8-stage ring) it
+//     issues four TMA loads on one barrier: a 128 x 128 A tile, a 64 x 128 B
+//     tile, and the stage's scale boxes sa[4 row tiles][4 K blocks] and
+//     sb[2 column tiles][4 K blocks].  Nothing on the producer waits for
+//     global memory, so it runs up to eight stages ahead.
 //   * warp 9: MMA issuer (lane 0).  Per stage, four MMAs (M=128, N=64, K=32,
 //     one per 32-wide K block) into the four 64-column TMEM partial buffers
 //     of one of two buffer sets; one commit hands the whole set over.
 //   * warps 0-7: promotion.  Warp w reads TMEM lanes 32(w%4).. (C rows) and
 //     columns 32(w/4)..+31 of each partial, exactly one 32 x 32 scale tile,
-//     so its scale is one number per K block (read as one 16-byte vector per
-//     stage).  Each thread keeps its row's 32 FP32 accumulators in
+//     so its scale is one number per K block: sa * sb from two 16-byte
+//     shared-memory vectors per stage.  Each thread keeps its row's 32 FP32 accumulators in
 //     registers and adds (sa*sb) * partial with FP32 FMAs, two K blocks'
 //     partials loaded per TMEM wait.  After the last stage of a tile it
 //     rounds to BF16 and stores 64 bytes.
 //   * A stage is recycled only when its MMAs have completed and all eight
-//     promotion warps have read its scale products (empty count 1 + 8); a
+//     promotion warps have read its scales (empty count 1 + 8); a
 //     partial-buffer set is reused once all eight warps hold its data in
 //     registers (pempty count 8).
 #include <cuda_bf16.h>
@@ -77,11 +77,16 @@ struct BsArgs {
 struct Lay {
   static constexpr int kABytes = BM * BK;
   static constexpr int kBBytes = BN * BK;
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kSaBytes = 4 * KPS * 4;
+  static constexpr int kSbBytes = 2 * KPS * 4;
+  static constexpr int kStageBytes = kABytes + kBBytes + kSaBytes + kSbBytes;
   static constexpr int kA = 0;
   static constexpr int kB = kA + STAGES * kABytes;
-  static constexpr int kScale = kB + STAGES * kBBytes;     // STAGES x 32 floats
-  static constexpr int kBar = kScale + STAGES * 32 * 4;
+  // Per stage: the A-scale box [4 row tiles][4 K blocks] (64 B) and the
+  // B-scale box [2 column tiles][4 K blocks] (32 B), in a 128-byte slot.
+  static constexpr int kScaleSlot = 128;
+  static constexpr int kScale = kB + STAGES * kBBytes;
+  static constexpr int kBar = kScale + STAGES * kScaleSlot;
   static constexpr int kNumBars = 2 * STAGES + 2 * NSETS + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kEnd = kMisc + 16;
@@ -102,6 +107,8 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n,
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_e4m3_block32_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmSa,
+                             const __grid_constant__ CUtensorMap tmSb,
                              const BsArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
@@ -117,7 +124,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto pfull_bar = [&](int p) { return bar0 + 8u * (2 * STAGES + p); };
   auto pempty_bar = [&](int p) { return bar0 + 8u * (2 * STAGES + NSETS + p); };
   const uint32_t final_bar = bar0 + 8u * (2 * STAGES + 2 * NSETS);
-  float *scales = reinterpret_cast<float *>(sbase + Lay::kScale);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + Lay::kMisc);
   volatile int *abort_flag =
       reinterpret_cast<volatile int *>(sbase + Lay::kMisc + 4);
@@ -126,8 +132,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tiles_n = (a.N + BN - 1) / BN;
   const int total_tiles = tiles_m * tiles_n;
   const int nks = (a.K + BK - 1) / BK;          // stages per tile
-  const int nkb = (a.K + KB - 1) / KB;          // scale blocks along K
-  const int srow_a = (a.M + 31) / 32, srow_b = (a.N + 31) / 32;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -145,6 +149,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmSa);
+    tma_prefetch_desc(&tmSb);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -170,24 +176,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        // Lane l: K block kb = 4ks + (l & 3) of scale tile
-        // (row tile q, column tile c) = ((l >> 3) & 3 ... ) laid out as
-        // scales[s][(q * 2 + c) * 4 + (kb & 3)], so that promotion warp
-        // (q, c) reads its stage's four products as one 16-byte vector.
-        const int k4 = lane & 3, c = (lane >> 2) & 1, q = lane >> 3;
-        const int kb = ks * KPS + k4;
-        const int rt = m0 / 32 + q, ct = n0 / 32 + c;
-        float v = 0.0f;
-        if (rt < srow_a && ct < srow_b && kb < nkb)
-          v = __fmul_rn(a.sa[rt * a.ld_sa + kb], a.sb[ct * a.ld_sb + kb]);
-        scales[s * 32 + (q * 2 + c) * 4 + k4] = v;
-        __syncwarp();
+        // Operand tiles and the stage's scale boxes, all on one barrier.
+        // TMA zero-fills scale entries past the grid's edge.
         if (lane == 0) {
-          mbar_arrive_expect_tx(full_bar(s), Lay::kStageBytes);
-          tma_load_2d(base + Lay::kA + s * Lay::kABytes, &tmA, full_bar(s),
-                      ks * BK, m0);
-          tma_load_2d(base + Lay::kB + s * Lay::kBBytes, &tmB, full_bar(s),
-                      ks * BK, n0);
+          const uint32_t fb = full_bar(s);
+          const uint32_t sslot = base + Lay::kScale + s * Lay::kScaleSlot;
+          mbar_arrive_expect_tx(fb, Lay::kStageBytes);
+          tma_load_2d(base + Lay::kA + s * Lay::kABytes, &tmA, fb, ks * BK, m0);
+          tma_load_2d(base + Lay::kB + s * Lay::kBBytes, &tmB, fb, ks * BK, n0);
+          tma_load_2d(sslot, &tmSa, fb, ks * KPS, m0 / 32);
+          tma_load_2d(sslot + Lay::kSaBytes, &tmSb, fb, ks * KPS, n0 / 32);
         }
         ++issued;
         if (++s == STAGES) { s = 0; ph ^= 1u; }
@@ -259,8 +257,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const float4 sc = *reinterpret_cast<const float4 *>(
-            scales + s * 32 + (q * 2 + c) * 4);
+        const float4 va = *reinterpret_cast<const float4 *>(
+            sbase + Lay::kScale + s * Lay::kScaleSlot + q * KPS * 4);
+        const float4 vb = *reinterpret_cast<const float4 *>(
+            sbase + Lay::kScale + s * Lay::kScaleSlot + Lay::kSaBytes +
+            c * KPS * 4);
+        const float4 sc = make_float4(__fmul_rn(va.x, vb.x), __fmul_rn(va.y, vb.y),
+                                      __fmul_rn(va.z, vb.z), __fmul_rn(va.w, vb.w));
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(s));
         if (++s == STAGES) { s = 0; ph ^= 1u; }
@@ -340,6 +343,21 @@ __global__ void zero_c_kernel_bs(uint16_t *C, int64_t ldc, int64_t M,
   }
 }
 
+bool encode_2d_f32(CUtensorMap *m, const void *ptr, uint64_t inner,
+                   uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                   uint32_t box_outer) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(ptr),
+             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_2d_bs(CUtensorMap *m, const void *ptr, uint64_t inner,
                   uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
                   uint32_t box_outer) {
@@ -379,7 +397,8 @@ extern "C" fp8la_status fp8_gemm_blockscaled_32x32(
   if (!A || !B || !sa || !sb || lda < K || ldb < K || ld_sa < nkb ||
       ld_sb < nkb)
     return FP8LA_ERR_INVALID_ARG;
-  if (!aligned16(A) || !aligned16(B) || lda % 16 != 0 || ldb % 16 != 0)
+  if (!aligned16(A) || !aligned16(B) || lda % 16 != 0 || ldb % 16 != 0 ||
+      !aligned16(sa) || !aligned16(sb) || ld_sa % 4 != 0 || ld_sb % 4 != 0)
     return FP8LA_ERR_ALIGNMENT;
   if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) ||
       K >= (int64_t(1) << 31) || lda >= (int64_t(1) << 39) ||
@@ -387,9 +406,11 @@ extern "C" fp8la_status fp8_gemm_blockscaled_32x32(
       ld_sb >= (int64_t(1) << 31))
     return FP8LA_ERR_UNSUPPORTED;
   if (!device_is_sm10x()) return FP8LA_ERR_UNSUPPORTED;
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tmSa, tmSb;
   if (!encode_2d_bs(&tmA, A, K, M, lda, BK, BM) ||
-      !encode_2d_bs(&tmB, B, K, N, ldb, BK, BN))
+      !encode_2d_bs(&tmB, B, K, N, ldb, BK, BN) ||
+      !encode_2d_f32(&tmSa, sa, nkb, (M + 31) / 32, ld_sa * 4, KPS, BM / 32) ||
+      !encode_2d_f32(&tmSb, sb, nkb, (N + 31) / 32, ld_sb * 4, KPS, BN / 32))
     return FP8LA_ERR_CUDA;
   unsigned *status = status_word_ptr();
   if (!status) return FP8LA_ERR_CUDA;
@@ -414,6 +435,7 @@ extern "C" fp8la_status fp8_gemm_blockscaled_32x32(
   if (sms <= 0) return FP8LA_ERR_CUDA;
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int grid = static_cast<int>(tiles < sms ? tiles : sms);
-  gemm_e4m3_block32_kernel<<<grid, kThreads, Lay::kAlloc, s>>>(tmA, tmB, args);
+  gemm_e4m3_block32_kernel<<<grid, kThreads, Lay::kAlloc, s>>>(tmA, tmB, tmSa,
+                                                               tmSb, args);
   return launch_status();
 }

@@ -69,6 +69,13 @@ def test_host_argument_rejection(lib):
     # M == 0 or N == 0 is a no-op that succeeds without touching the GPU
     assert lib.fp8_gemm(None, 16, None, 16, None, 8, 0, 8, 16, None, None, None) == 0
     assert lib.fp8_gemm(None, 16, None, 16, None, 8, 8, 0, 16, None, None, None) == 0
+    # block-scaled: scale grids must allow 16-byte TMA rows
+    assert lib.fp8_gemm_blockscaled_32x32(one, 64, one, 64, one, 64, 64, 64, 64,
+                                          one, 2, one, 4, None) == -2
+    assert lib.fp8_gemm_blockscaled_32x32(one, 64, one, 64, one, 64, 64, 64, 64,
+                                          P(20), 4, one, 4, None) == -2
+    assert lib.fp8_gemm_blockscaled_32x32(one, 64, one, 64, one, 64, 64, 64, 64,
+                                          one, 1, one, 4, None) == -1
     # grouped: group count out of range, NULL offsets
     assert lib.fp8_grouped_gemm(0, one, 8, one, 16, one, 16, 256, one, 8, 8, 16, one, one, None) == -1
     assert lib.fp8_grouped_gemm(2000, one, 8, one, 16, one, 16, 256, one, 8, 8, 16, one, one, None) == -1

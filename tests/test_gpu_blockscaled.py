@@ -53,12 +53,22 @@ def _run(fl, A, B, sa, sb, ldc_pad=0):
     dB[:, :K] = to_dev(B)
     Cs = torch.full((M, N + ldc_pad), 5.0, dtype=torch.bfloat16, device="cuda")
     C = Cs[:, :N]
-    fl.gemm_blockscaled_32x32(dA[:, :K], dB[:, :K], to_dev(sa), to_dev(sb), C=C)
+    fl.gemm_blockscaled_32x32(dA[:, :K], dB[:, :K], _dev_scales(sa), _dev_scales(sb), C=C)
     torch.cuda.synchronize()
     assert fl.device_status() == 0
     if ldc_pad:
         assert torch.all(Cs[:, N:] == 5.0)
     return bf16_to_f64(C.contiguous())
+
+
+def _dev_scales(s):
+    """Scale grid on the device with its leading dimension padded to a
+    multiple of 4 floats (the GEMM reads it by TMA)."""
+    import torch
+    r, c = s.shape
+    d = torch.full((r, (c + 3) // 4 * 4), float("nan"), dtype=torch.float32, device="cuda")
+    d[:, :c] = to_dev(s)
+    return d[:, :c]
 
 
 def _scales(rng, rows, K):
@@ -99,6 +109,7 @@ def test_one_hot_k_block():
     sa = np.zeros((4, 8), np.float32)
     sb = np.ones((4, 8), np.float32)
     sa[:, 3] = 0.5
+    # (N = 128 here, so sb has 4 column-tile rows)
     got = _run(fl, A, B, sa, sb)
     check_pertensor(got, A[:, 96:128], B[:, 96:128], np.float32(0.5), np.float32(1),
                     what="one-hot")
