@@ -5,7 +5,12 @@ fp32, N(0,1) with 0.1% +-50 sigma outliers) and B (N(0,0.02), same outlier
 rule) to E4M3 on the device (amax -> scale -> cast), then the scaled GEMM
 with FP32 accumulation and BF16 output.  Inputs are generated once (seeded),
 copied to HBM before timing.  `value` is 2*M*N*K / (time of one whole step),
-in TFLOP/s; the roofline object describes the GEMM kernel alone.
+in TFLOP/s; the roofline object describes the GEMM kernel alone.  By default
+consecutive steps are pipelined: the HBM-bound quantisation of step i+1 runs
+on a second stream while the tensor-bound GEMM of step i runs (codes and
+scales double-buffered); every step still does all of its work, and the
+serial schedule's time is reported beside it (--schedule serial times it
+alone).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -278,7 +283,44 @@ def _workload_pertensor(fl, torch, dev, sptr, ph):
                     P(scale, 0), P(scale, 1), sptr)
         ph.mark("gemm")
 
-    return dict(step=step, flops=FLOPS, launches=5, workload=WORKLOAD,
+    # Pipelined schedule: step i+1's quantisation (HBM-bound) runs on its own
+    # stream while step i's GEMM (tensor-bound) runs on another.  Codes and
+    # scales are double-buffered; events order quantize(i) before GEMM(i)
+    # and GEMM(i) before quantize(i+2), which reuses its buffers.
+    main = torch.cuda.current_stream(dev)
+    sq, sg = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    qa2 = [qa, torch.empty_like(qa)]
+    qb2 = [qb, torch.empty_like(qb)]
+    amax2 = torch.empty(4, dtype=torch.float32, device=dev)
+    scale2 = torch.empty(4, dtype=torch.float32, device=dev)
+    qdone = [torch.cuda.Event(), torch.cuda.Event()]
+    gdone = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def pbegin():
+        for e in qdone + gdone:
+            e.record(main)
+        sq.wait_stream(main)
+        sg.wait_stream(main)
+
+    def pstep(i):
+        b = i & 1
+        sq.wait_event(gdone[b])
+        fl.fp8_quantize_pertensor(P(A), N_SIZE, N_SIZE, N_SIZE, P(qa2[b]), N_SIZE,
+                                  P(amax2, 2 * b), P(scale2, 2 * b), sq.cuda_stream)
+        fl.fp8_quantize_pertensor(P(B), N_SIZE, N_SIZE, N_SIZE, P(qb2[b]), N_SIZE,
+                                  P(amax2, 2 * b + 1), P(scale2, 2 * b + 1), sq.cuda_stream)
+        qdone[b].record(sq)
+        sg.wait_event(qdone[b])
+        fl.fp8_gemm(P(qa2[b]), N_SIZE, P(qb2[b]), N_SIZE, P(C), N_SIZE, N_SIZE, N_SIZE,
+                    N_SIZE, P(scale2, 2 * b), P(scale2, 2 * b + 1), sg.cuda_stream)
+        gdone[b].record(sg)
+
+    def pend():
+        main.wait_stream(sq)
+        main.wait_stream(sg)
+
+    return dict(step=step, pipeline=(pbegin, pstep, pend), flops=FLOPS, launches=5,
+                workload=WORKLOAD,
                 config={"M": N_SIZE, "N": N_SIZE, "K": N_SIZE,
                         "l2": "inputs 2 x 268 MB fp32 > 129 MB L2; no flush"},
                 inputs=[(A, A_np), (B, B_np)], outputs=[C],
@@ -436,11 +478,35 @@ def run_gpu(args):
     torch.cuda.synchronize()
     sampler.start()
     time.sleep(0.3)
+    pipelined = args.schedule == "pipelined" and "pipeline" in W
+    serial_ms = None
+    if pipelined:
+        # The serial schedule too, for reference (same steps, one stream).
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(args.steps):
+            step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        serial_ms = s0.elapsed_time(s1) / args.steps
+        pbegin, pstep, pend = W["pipeline"]
+        pbegin()
+        for i in range(max(3, args.warmup)):
+            pstep(i)
+        pend()
+        torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for _ in range(args.steps):
-        step()
+    if pipelined:
+        pbegin()
+        for i in range(args.steps):
+            pstep(i)
+        pend()
+    else:
+        for _ in range(args.steps):
+            step()
     t1.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
@@ -515,7 +581,11 @@ def run_gpu(args):
                                   "algorithmic_bytes_per_elem":
                                       5 if args.workload == "blockscaled" else QUANT_BYTES_PER_ELEM},
             "breakdown": {"gemm_ms": g_avg, "quantize_ms": q_avg,
-                          "gemm_tflops": gemm_tflops, "quantize_gbs": quant_gbs},
+                          "gemm_tflops": gemm_tflops, "quantize_gbs": quant_gbs,
+                          "schedule": "pipelined" if pipelined else "serial",
+                          "serial_ms_per_step": serial_ms if pipelined else ms_step,
+                          "serial_value": (world * W["flops"] / (serial_ms * 1e-3) / 1e12
+                                           if pipelined else value)},
             "e2e": {"value": world * W["flops"] / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms},
@@ -543,6 +613,9 @@ def main():
     ap.add_argument("--workload", default="pertensor8192", choices=sorted(WORKLOADS),
                     help="pertensor8192 is the headline line; the others measure the "
                          "block-scaled and grouped variants")
+    ap.add_argument("--schedule", default="pipelined", choices=["pipelined", "serial"],
+                    help="pipelined (default): step i+1's quantisation overlaps step i's GEMM "
+                         "on a second stream; serial: one stream, steps back to back")
     ap.add_argument("--linears", default="",
                     help="blockscaled only: comma list of qkv,attn_out,gate_up,down "
                          "(default: all four)")

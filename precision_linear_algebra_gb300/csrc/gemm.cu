@@ -80,6 +80,11 @@ struct Smem {
   static constexpr int kAlloc = kEnd + 1024;  // slack for aligning the base
 };
 
+// TMA destinations: operand tiles start on their 1024-byte swizzle atoms.
+static_assert(Smem<256, 4>::kB % 1024 == 0 && Smem<256, 4>::kBBytes % 1024 == 0,
+              "B tiles");
+static_assert(Smem<256, 4>::kAlloc <= 227 * 1024, "shared memory");
+
 // Tile t of a tiles_m x tiles_n grid in grouped order.
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n,
                                             int &mb, int &nb) {
@@ -396,6 +401,11 @@ struct PairSmem {
   static constexpr int kEnd = kPrefix + (kMaxGroups + 1) * 4;
   static constexpr int kAlloc = kEnd + 1024;
 };
+
+static_assert(PairSmem::kB % 1024 == 0 && PairSmem::kABytes % 1024 == 0 &&
+                  PairSmem::kBBytes % 1024 == 0 && PairSmem::kBar % 8 == 0,
+              "pair layout");
+static_assert(PairSmem::kAlloc <= 227 * 1024, "shared memory");
 
 template <bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1)

@@ -82,9 +82,11 @@ struct Lay {
   static constexpr int kStageBytes = kABytes + kBBytes + kSaBytes + kSbBytes;
   static constexpr int kA = 0;
   static constexpr int kB = kA + STAGES * kABytes;
-  // Per stage: the A-scale box [4 row tiles][4 K blocks] (64 B) and the
-  // B-scale box [2 column tiles][4 K blocks] (32 B), in a 128-byte slot.
-  static constexpr int kScaleSlot = 128;
+  // Per stage: the A-scale box [4 row tiles][4 K blocks] (64 B) at +0 and
+  // the B-scale box [2 column tiles][4 K blocks] (32 B) at +128.  Every TMA
+  // destination in shared memory starts on a 128-byte boundary.
+  static constexpr int kSbOffset = 128;
+  static constexpr int kScaleSlot = 256;
   static constexpr int kScale = kB + STAGES * kBBytes;
   static constexpr int kBar = kScale + STAGES * kScaleSlot;
   static constexpr int kNumBars = 2 * STAGES + 2 * NSETS + 1;
@@ -92,6 +94,18 @@ struct Lay {
   static constexpr int kEnd = kMisc + 16;
   static constexpr int kAlloc = kEnd + 1024;
 };
+
+// TMA writes to shared memory must start on 128-byte boundaries (the
+// swizzled operand tiles additionally on their 1024-byte swizzle atoms).
+static_assert(Lay::kA % 1024 == 0 && Lay::kABytes % 1024 == 0, "A tiles");
+static_assert(Lay::kB % 1024 == 0 && Lay::kBBytes % 1024 == 0, "B tiles");
+static_assert(Lay::kScale % 128 == 0 && Lay::kScaleSlot % 128 == 0 &&
+                  Lay::kSbOffset % 128 == 0 &&
+                  Lay::kSbOffset >= Lay::kSaBytes &&
+                  Lay::kSbOffset + Lay::kSbBytes <= Lay::kScaleSlot,
+              "scale boxes");
+static_assert(Lay::kBar % 8 == 0, "mbarriers");
+static_assert(Lay::kAlloc <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n,
                                             int &mb, int &nb) {
@@ -185,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(base + Lay::kA + s * Lay::kABytes, &tmA, fb, ks * BK, m0);
           tma_load_2d(base + Lay::kB + s * Lay::kBBytes, &tmB, fb, ks * BK, n0);
           tma_load_2d(sslot, &tmSa, fb, ks * KPS, m0 / 32);
-          tma_load_2d(sslot + Lay::kSaBytes, &tmSb, fb, ks * KPS, n0 / 32);
+          tma_load_2d(sslot + Lay::kSbOffset, &tmSb, fb, ks * KPS, n0 / 32);
         }
         ++issued;
         if (++s == STAGES) { s = 0; ph ^= 1u; }
@@ -260,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float4 va = *reinterpret_cast<const float4 *>(
             sbase + Lay::kScale + s * Lay::kScaleSlot + q * KPS * 4);
         const float4 vb = *reinterpret_cast<const float4 *>(
-            sbase + Lay::kScale + s * Lay::kScaleSlot + Lay::kSaBytes +
+            sbase + Lay::kScale + s * Lay::kScaleSlot + Lay::kSbOffset +
             c * KPS * 4);
         const float4 sc = make_float4(__fmul_rn(va.x, vb.x), __fmul_rn(va.y, vb.y),
                                       __fmul_rn(va.z, vb.z), __fmul_rn(va.w, vb.w));
