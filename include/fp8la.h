@@ -93,6 +93,30 @@ FP8LA_API fp8la_status fp8_quantize_pertensor(const float *x, int64_t rows, int6
                                     fp8la_stream_t stream);
 
 /*
+ * FP8 formats for the *_ex entry points.  E4M3 is the method's format;
+ * E5M2 ([P3] tensor-core paragraph names both; [FP8]: 1 sign, 5 exponent
+ * bits with bias 15, 2 mantissa bits, IEEE-style infinities and NaNs,
+ * largest finite magnitude 57344) trades precision for range.
+ */
+#define FP8LA_FORMAT_E4M3 0
+#define FP8LA_FORMAT_E5M2 1
+
+/*
+ * fp8_quantize_pertensor for a chosen FP8 format: as above with 448
+ * replaced by the format's largest finite magnitude (57344 for E5M2):
+ * qscale = fp32(fmax / amax), scale = fp32(amax / fmax), saturating RNE
+ * cast to the format (NaN -> 0x7F).  format: FP8LA_FORMAT_E4M3 or
+ * FP8LA_FORMAT_E5M2, else FP8LA_ERR_INVALID_ARG.
+ */
+FP8LA_API fp8la_status fp8_quantize_pertensor_ex(const float *x, int64_t rows,
+                                                 int64_t cols, int64_t ldx,
+                                                 uint8_t *q, int64_t ldq,
+                                                 float *amax_out,
+                                                 float *scale_out,
+                                                 int32_t format,
+                                                 fp8la_stream_t stream);
+
+/*
  * 32x32 block E4M3 quantisation ([P3] implementation paragraph: scale
  * granularity of 32x32 blocks).  Each 32x32 tile (ragged at the right and
  * bottom edges: a tile covers only its in-range elements) is quantised
@@ -126,6 +150,19 @@ FP8LA_API fp8la_status fp8_gemm(const uint8_t *A, int64_t lda, const uint8_t *B,
                       int64_t ldb, uint16_t *C, int64_t ldc, int64_t M,
                       int64_t N, int64_t K, const float *scale_a,
                       const float *scale_b, fp8la_stream_t stream);
+
+/*
+ * fp8_gemm with each operand in a chosen FP8 format (FP8LA_FORMAT_E4M3 or
+ * FP8LA_FORMAT_E5M2; the two may differ): the same contraction, FP32
+ * accumulation and BF16 output, decoding A with a_format and B with
+ * b_format.  Other format values return FP8LA_ERR_INVALID_ARG.
+ */
+FP8LA_API fp8la_status fp8_gemm_ex(const uint8_t *A, int64_t lda,
+                                   const uint8_t *B, int64_t ldb, uint16_t *C,
+                                   int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                   const float *scale_a, const float *scale_b,
+                                   int32_t a_format, int32_t b_format,
+                                   fp8la_stream_t stream);
 
 /*
  * 32x32 block-scaled E4M3 GEMM ([P3] implementation paragraph: 32x32 scale

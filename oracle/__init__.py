@@ -28,7 +28,8 @@ Sources cited in the docstrings (the three web pages this method comes from):
      ("要落地这些优化"), monitoring, checklist, conclusion.
 [FP8] Micikevicius et al., "FP8 Formats for Deep Learning" (2022): the E4M3
      encoding that [P1] calls ``float8e4m3fn`` (bias 7, no infinities, a
-     single NaN mantissa pattern, max 448).
+     single NaN mantissa pattern, max 448), and E5M2 (bias 15, IEEE-style
+     infinities and NaNs, max 57344), the second format [P3] names.
 
 Parity pins: every function here is pinned by ``tests/test_oracle_*.py``
 against facts that do not come from this code (the format's fixed values,
@@ -37,6 +38,7 @@ No function is "parity unpinned".
 """
 
 from .e4m3 import decode_code, decode, encode, E4M3_MAX, NAN_CODE
+from . import e5m2
 from .bf16 import bf16_rne, bf16_bits_to_float
 from .quantize import (amax_fp32, scales_from_amax, quantize_pertensor,
                        quantize_blockwise_32x32)
@@ -44,7 +46,7 @@ from .gemm import (gemm_pertensor, gemm_blockscaled_32x32, gemm_grouped,
                    bound_pertensor, bound_blockscaled_32x32)
 
 __all__ = [
-    "decode_code", "decode", "encode", "E4M3_MAX", "NAN_CODE",
+    "decode_code", "decode", "encode", "E4M3_MAX", "NAN_CODE", "e5m2",
     "bf16_rne", "bf16_bits_to_float",
     "amax_fp32", "scales_from_amax", "quantize_pertensor",
     "quantize_blockwise_32x32",

@@ -25,8 +25,11 @@ and C its bf16 RNE rounding as uint16 bit patterns.
 
 import numpy as np
 
+from . import e4m3, e5m2
 from .e4m3 import decode
 from .bf16 import bf16_rne
+
+DECODERS = {"e4m3": e4m3.decode, "e5m2": e5m2.decode}
 
 KMAX_EXACT = 1 << 17
 
@@ -37,12 +40,17 @@ def _rows_cols(M, N, rows, cols):
     return rows, cols
 
 
-def gemm_pertensor(A, B, scale_a, scale_b, rows=None, cols=None):
+def gemm_pertensor(A, B, scale_a, scale_b, rows=None, cols=None,
+                   a_fmt="e4m3", b_fmt="e4m3"):
     """C[m, n] = bf16_RNE(sa * sb * sum_k dec(A[m, k]) * dec(B[n, k])).
 
     FP32 accumulation is the kernel's choice ([P1], parameter list "累加器
     FP32"); the oracle sums exactly instead (see the module docstring).
-    ``rows``/``cols`` restrict the result to C[rows][:, cols].
+    ``rows``/``cols`` restrict the result to C[rows][:, cols].  a_fmt,
+    b_fmt select each operand's FP8 format ("e4m3" or "e5m2").  With an E5M2
+    operand the products span more than 53 bits, so the fp64 sum is exact
+    only up to a relative rounding of 2^-53 per addition -- 2^-31 of the
+    accumulation term of the error bound.
     """
     A = np.asarray(A, dtype=np.uint8)
     B = np.asarray(B, dtype=np.uint8)
@@ -53,9 +61,9 @@ def gemm_pertensor(A, B, scale_a, scale_b, rows=None, cols=None):
     if K >= KMAX_EXACT:
         raise ValueError("K too large for an exact fp64 sum")
     rows, cols = _rows_cols(M, N, rows, cols)
-    Ad = decode(A[rows])                       # [m][k], fp64
-    Bd = decode(B[cols])                       # [n][k], fp64
-    S = Ad @ Bd.T                              # exact
+    Ad = DECODERS[a_fmt](A[rows])              # [m][k], fp64
+    Bd = DECODERS[b_fmt](B[cols])              # [n][k], fp64
+    S = Ad @ Bd.T                              # exact (E4M3 x E4M3)
     r = (np.float64(np.float32(scale_a)) * np.float64(np.float32(scale_b))) * S
     return r, bf16_rne(r)
 

@@ -10,7 +10,8 @@ The steps, in the order the method takes them:
 1. amax = max_i |x_i| over the tensor (or tile), NaN ignored, in fp32.
    Max is exact, so the order of the reduction does not matter.
 2. qscale = fp32(448 / amax), the multiplier applied before the cast, and
-   scale  = fp32(amax / 448), the dequantisation factor the GEMM consumes.
+   scale  = fp32(amax / 448), the dequantisation factor the GEMM consumes
+   (57344 in place of 448 for the E5M2 variant).
    Both are single IEEE fp32 divisions; neither is derived from the other.
    If amax == 0 or qscale is not finite, qscale = scale = 1.
 3. q_i = E4M3_RNE_satfinite(fp32(x_i * qscale)): one fp32 multiply, then the
@@ -19,9 +20,11 @@ The steps, in the order the method takes them:
 
 import numpy as np
 
-from .e4m3 import encode, E4M3_MAX
+from . import e4m3, e5m2
 
-_F448 = np.float32(E4M3_MAX)
+# format -> (largest finite magnitude, saturating RNE encoder)
+FORMATS = {"e4m3": (e4m3.E4M3_MAX, e4m3.encode),
+           "e5m2": (e5m2.E5M2_MAX, e5m2.encode)}
 
 
 def amax_fp32(x):
@@ -34,28 +37,32 @@ def amax_fp32(x):
     return np.float32(a.max())
 
 
-def scales_from_amax(amax):
-    """(qscale, scale) as fp32 scalars, by the two IEEE fp32 divisions."""
+def scales_from_amax(amax, fmt="e4m3"):
+    """(qscale, scale) as fp32 scalars, by the two IEEE fp32 divisions
+    qscale = fmax / amax and scale = amax / fmax (fmax = 448 for E4M3, 57344
+    for E5M2)."""
     amax = np.float32(amax)
+    fmax = np.float32(FORMATS[fmt][0])
     with np.errstate(divide="ignore", over="ignore", invalid="ignore"):
-        qscale = np.float32(_F448 / amax)
-        scale = np.float32(amax / _F448)
+        qscale = np.float32(fmax / amax)
+        scale = np.float32(amax / fmax)
     if amax == 0 or not np.isfinite(qscale):
         return np.float32(1.0), np.float32(1.0)
     return qscale, scale
 
 
-def quantize_pertensor(x):
+def quantize_pertensor(x, fmt="e4m3"):
     """Quantise an fp32 array with one per-tensor scale.
 
-    Returns (codes uint8 with x's shape, amax fp32, scale fp32).
+    Returns (codes uint8 with x's shape, amax fp32, scale fp32).  fmt is
+    "e4m3" (the method's format) or "e5m2".
     """
     x = np.asarray(x, dtype=np.float32)
     amax = amax_fp32(x)
-    qscale, scale = scales_from_amax(amax)
+    qscale, scale = scales_from_amax(amax, fmt)
     with np.errstate(over="ignore", invalid="ignore"):
         y = (x * qscale).astype(np.float32)      # fp32 * fp32 -> fp32, RNE
-    return encode(y), amax, scale
+    return FORMATS[fmt][1](y), amax, scale
 
 
 def quantize_blockwise_32x32(x):

@@ -23,6 +23,9 @@ FP8LA_ERR_ALIGNMENT = -2
 FP8LA_ERR_UNSUPPORTED = -3
 FP8LA_ERR_CUDA = -4
 FP8LA_ERR_DEVICE_TIMEOUT = -5
+FP8LA_FORMAT_E4M3 = 0
+FP8LA_FORMAT_E5M2 = 1
+_FORMATS = {"e4m3": FP8LA_FORMAT_E4M3, "e5m2": FP8LA_FORMAT_E5M2}
 
 # (name, restype, argtypes) of every entry point in include/fp8la.h.
 _P = ctypes.c_void_p
@@ -31,8 +34,10 @@ _I32 = ctypes.c_int32
 _S = ctypes.c_int
 SIGNATURES = [
     ("fp8_quantize_pertensor", _S, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P]),
+    ("fp8_quantize_pertensor_ex", _S, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _I32, _P]),
     ("fp8_quantize_blockwise_32x32", _S, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P]),
     ("fp8_gemm", _S, [_P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P, _P]),
+    ("fp8_gemm_ex", _S, [_P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P, _I32, _I32, _P]),
     ("fp8_gemm_blockscaled_32x32", _S,
      [_P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _I64, _P, _I64, _P]),
     ("fp8_grouped_gemm", _S,
@@ -94,6 +99,16 @@ def fp8_quantize_pertensor(x, rows, cols, ldx, q, ldq, amax_out, scale_out, stre
                  scale_out, stream)
 
 
+def fp8_quantize_pertensor_ex(x, rows, cols, ldx, q, ldq, amax_out, scale_out, fmt, stream):
+    return _call("fp8_quantize_pertensor_ex", x, rows, cols, ldx, q, ldq, amax_out,
+                 scale_out, fmt, stream)
+
+
+def fp8_gemm_ex(A, lda, B, ldb, C, ldc, M, N, K, scale_a, scale_b, a_fmt, b_fmt, stream):
+    return _call("fp8_gemm_ex", A, lda, B, ldb, C, ldc, M, N, K, scale_a, scale_b,
+                 a_fmt, b_fmt, stream)
+
+
 def fp8_quantize_blockwise_32x32(x, rows, cols, ldx, q, ldq, scales, ld_scales, stream):
     return _call("fp8_quantize_blockwise_32x32", x, rows, cols, ldx, q, ldq,
                  scales, ld_scales, stream)
@@ -148,11 +163,11 @@ def _ptr(t):
     return t.data_ptr() if t is not None else None
 
 
-def quantize_pertensor(x, q=None, amax=None, scale=None):
+def quantize_pertensor(x, q=None, amax=None, scale=None, fmt="e4m3"):
     """x: fp32 CUDA [rows][cols] (row stride may exceed cols).
 
     Returns (q uint8 [rows][cols], amax fp32 [1], scale fp32 [1]), all on
-    x's device; nothing is synchronised.
+    x's device; nothing is synchronised.  fmt: "e4m3" or "e5m2".
     """
     import torch
     assert x.dtype == torch.float32 and x.dim() == 2 and x.stride(1) == 1
@@ -161,8 +176,8 @@ def quantize_pertensor(x, q=None, amax=None, scale=None):
         q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
     amax = torch.empty(1, dtype=torch.float32, device=x.device) if amax is None else amax
     scale = torch.empty(1, dtype=torch.float32, device=x.device) if scale is None else scale
-    fp8_quantize_pertensor(_ptr(x), rows, cols, x.stride(0), _ptr(q), q.stride(0),
-                           _ptr(amax), _ptr(scale), _stream())
+    fp8_quantize_pertensor_ex(_ptr(x), rows, cols, x.stride(0), _ptr(q), q.stride(0),
+                              _ptr(amax), _ptr(scale), _FORMATS[fmt], _stream())
     return q, amax, scale
 
 
@@ -184,15 +199,22 @@ def quantize_blockwise_32x32(x, q=None, scales=None):
     return q, scales
 
 
-def gemm(A, B, scale_a, scale_b, C=None):
-    """A uint8 [M][K], B uint8 [N][K] (K-major), scales fp32 [1] -> C bf16 [M][N]."""
+def gemm(A, B, scale_a, scale_b, C=None, a_fmt="e4m3", b_fmt="e4m3"):
+    """A uint8 [M][K], B uint8 [N][K] (K-major), scales fp32 [1] -> C bf16 [M][N].
+
+    a_fmt, b_fmt: "e4m3" (default, fp8_gemm) or "e5m2" (fp8_gemm_ex)."""
     import torch
     M, K = A.shape
     N = B.shape[0]
     if C is None:
         C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
-    fp8_gemm(_ptr(A), A.stride(0), _ptr(B), B.stride(0), _ptr(C), C.stride(0),
-             M, N, K, _ptr(scale_a), _ptr(scale_b), _stream())
+    if a_fmt == "e4m3" and b_fmt == "e4m3":
+        fp8_gemm(_ptr(A), A.stride(0), _ptr(B), B.stride(0), _ptr(C), C.stride(0),
+                 M, N, K, _ptr(scale_a), _ptr(scale_b), _stream())
+    else:
+        fp8_gemm_ex(_ptr(A), A.stride(0), _ptr(B), B.stride(0), _ptr(C), C.stride(0),
+                    M, N, K, _ptr(scale_a), _ptr(scale_b), _FORMATS[a_fmt],
+                    _FORMATS[b_fmt], _stream())
     return C
 
 

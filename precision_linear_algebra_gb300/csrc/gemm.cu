@@ -61,6 +61,7 @@ struct GemmArgs {
   uint64_t timeout_ns;
   int32_t withhold_first;  // diagnostic: skip the first TMA arrival
   int32_t c_vec16;         // C rows allow 16-byte stores (C 16-byte aligned, ldc % 8 == 0)
+  uint32_t fmt_bits;       // operand-format bits of the MMA instruction descriptor
 };
 
 template <int BN, int STAGES>
@@ -286,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 5) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+      const uint32_t idesc = idesc_e4m3_f32(BM, BN) | a.fmt_bits;
       uint32_t s = 0, ph = 0;
       uint32_t local = 0;
       bool ok = true;
@@ -526,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 5) {
     // ------------------------------------------------- MMA (leader CTA only)
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = idesc_e4m3_f32(P_BM, P_BN);
+      const uint32_t idesc = idesc_e4m3_f32(P_BM, P_BN) | a.fmt_bits;
       uint32_t s = 0, ph = 0, local = 0;
       bool ok = true;
       for (int t = cluster_id; ok && t < total_tiles;
@@ -744,7 +745,8 @@ fp8la_status gemm_pertensor_impl(const uint8_t *A, int64_t lda,
                                  const uint8_t *B, int64_t ldb, uint16_t *C,
                                  int64_t ldc, int64_t M, int64_t N, int64_t K,
                                  const float *scale_a, const float *scale_b,
-                                 cudaStream_t s, int withhold) {
+                                 cudaStream_t s, int withhold,
+                                 uint32_t fmt_bits = 0) {
   fp8la_status st = check_operands(A, lda, B, ldb, C, ldc, M, N, K);
   if (st != FP8LA_OK) return st;
   if (M == 0 || N == 0) return FP8LA_OK;
@@ -778,6 +780,7 @@ fp8la_status gemm_pertensor_impl(const uint8_t *A, int64_t lda,
   args.timeout_ns = wait_timeout_ns();
   args.withhold_first = withhold;
   args.c_vec16 = aligned16(C) && ldc % 8 == 0;
+  args.fmt_bits = fmt_bits;
   if (pair) {
     const int64_t tiles = ((M + P_BM - 1) / P_BM) * ((N + P_BN - 1) / P_BN);
     return launch_gemm_pair<false>(tmA, tmB, args, tiles, s);
@@ -799,6 +802,24 @@ extern "C" fp8la_status fp8_gemm(const uint8_t *A, int64_t lda,
   return gemm_pertensor_impl(A, lda, B, ldb, C, ldc, M, N, K, scale_a,
                              scale_b, reinterpret_cast<cudaStream_t>(stream),
                              0);
+}
+
+extern "C" fp8la_status fp8_gemm_ex(const uint8_t *A, int64_t lda,
+                                    const uint8_t *B, int64_t ldb, uint16_t *C,
+                                    int64_t ldc, int64_t M, int64_t N,
+                                    int64_t K, const float *scale_a,
+                                    const float *scale_b, int32_t a_format,
+                                    int32_t b_format, fp8la_stream_t stream) {
+  const auto ok = [](int32_t f) {
+    return f == FP8LA_FORMAT_E4M3 || f == FP8LA_FORMAT_E5M2;
+  };
+  if (!ok(a_format) || !ok(b_format)) return FP8LA_ERR_INVALID_ARG;
+  // kind::f8f6f4 format codes: E4M3 = 0, E5M2 = 1 (A at bits 7-9, B at 10-12).
+  const uint32_t bits = (static_cast<uint32_t>(a_format) << 7) |
+                        (static_cast<uint32_t>(b_format) << 10);
+  return gemm_pertensor_impl(A, lda, B, ldb, C, ldc, M, N, K, scale_a,
+                             scale_b, reinterpret_cast<cudaStream_t>(stream),
+                             0, bits);
 }
 
 extern "C" fp8la_status fp8la_diag_gemm_withheld_arrival(

@@ -32,8 +32,9 @@
 //     columns 32(w/4)..+31 of each partial, exactly one 32 x 32 scale tile,
 //     so its scale is one number per K block: sa * sb from two 16-byte
 //     shared-memory vectors per stage.  Each thread keeps its row's 32 FP32 accumulators in
-//     registers and adds (sa*sb) * partial with FP32 FMAs, two K blocks'
-//     partials loaded per TMEM wait.  After the last stage of a tile it
+//     registers (as 16 packed pairs) and adds (sa*sb) * partial with packed
+//     FMAs (fma.rn.f32x2), two K blocks' partials per TMEM wait, each pair
+//     of K blocks in one asm statement.  After the last stage of a tile it
 //     rounds to BF16 and stores 64 bytes.
 //   * A stage is recycled only when its MMAs have completed and all eight
 //     promotion warps have read its scales (empty count 1 + 8); a
@@ -116,6 +117,64 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n,
   const int r = t - g * per_group;
   mb = first_m + r % gm;
   nb = r / gm;
+}
+
+// Promotion of two K blocks' partials (32 columns each, one lane row):
+// loads both from TMEM, waits, and adds s0 * first + s1 * second into the
+// 32 FP32 accumulators held as 16 packed pairs (acc[j] = columns 2j, 2j+1),
+// with packed FMAs fma.rn.f32x2 (each lane of a pair rounded once).  One
+// asm statement, so the loaded values never leave it.
+__device__ __forceinline__ void promote_pair(uint64_t (&acc)[16],
+                                             uint32_t taddr0, uint32_t taddr1,
+                                             float s0, float s1) {
+  asm volatile(
+      "{\n\t"
+      ".reg .b32 p<64>;\n\t"
+      ".reg .b64 q, sa, sb;\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {p0, p1, p2, p3, p4, p5, p6, p7, p8, p9, p10, p11, p12, p13, p14, p15, p16, p17, p18, p19, p20, p21, p22, p23, p24, p25, p26, p27, p28, p29, p30, p31}, [%16];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {p32, p33, p34, p35, p36, p37, p38, p39, p40, p41, p42, p43, p44, p45, p46, p47, p48, p49, p50, p51, p52, p53, p54, p55, p56, p57, p58, p59, p60, p61, p62, p63}, [%17];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n\t"
+      "mov.b64 sa, {%18, %18};\n\t"
+      "mov.b64 sb, {%19, %19};\n\t"
+      "mov.b64 q, {p0, p1};\n\tfma.rn.f32x2 %0, sa, q, %0;\n\t"
+      "mov.b64 q, {p2, p3};\n\tfma.rn.f32x2 %1, sa, q, %1;\n\t"
+      "mov.b64 q, {p4, p5};\n\tfma.rn.f32x2 %2, sa, q, %2;\n\t"
+      "mov.b64 q, {p6, p7};\n\tfma.rn.f32x2 %3, sa, q, %3;\n\t"
+      "mov.b64 q, {p8, p9};\n\tfma.rn.f32x2 %4, sa, q, %4;\n\t"
+      "mov.b64 q, {p10, p11};\n\tfma.rn.f32x2 %5, sa, q, %5;\n\t"
+      "mov.b64 q, {p12, p13};\n\tfma.rn.f32x2 %6, sa, q, %6;\n\t"
+      "mov.b64 q, {p14, p15};\n\tfma.rn.f32x2 %7, sa, q, %7;\n\t"
+      "mov.b64 q, {p16, p17};\n\tfma.rn.f32x2 %8, sa, q, %8;\n\t"
+      "mov.b64 q, {p18, p19};\n\tfma.rn.f32x2 %9, sa, q, %9;\n\t"
+      "mov.b64 q, {p20, p21};\n\tfma.rn.f32x2 %10, sa, q, %10;\n\t"
+      "mov.b64 q, {p22, p23};\n\tfma.rn.f32x2 %11, sa, q, %11;\n\t"
+      "mov.b64 q, {p24, p25};\n\tfma.rn.f32x2 %12, sa, q, %12;\n\t"
+      "mov.b64 q, {p26, p27};\n\tfma.rn.f32x2 %13, sa, q, %13;\n\t"
+      "mov.b64 q, {p28, p29};\n\tfma.rn.f32x2 %14, sa, q, %14;\n\t"
+      "mov.b64 q, {p30, p31};\n\tfma.rn.f32x2 %15, sa, q, %15;\n\t"
+      "mov.b64 q, {p32, p33};\n\tfma.rn.f32x2 %0, sb, q, %0;\n\t"
+      "mov.b64 q, {p34, p35};\n\tfma.rn.f32x2 %1, sb, q, %1;\n\t"
+      "mov.b64 q, {p36, p37};\n\tfma.rn.f32x2 %2, sb, q, %2;\n\t"
+      "mov.b64 q, {p38, p39};\n\tfma.rn.f32x2 %3, sb, q, %3;\n\t"
+      "mov.b64 q, {p40, p41};\n\tfma.rn.f32x2 %4, sb, q, %4;\n\t"
+      "mov.b64 q, {p42, p43};\n\tfma.rn.f32x2 %5, sb, q, %5;\n\t"
+      "mov.b64 q, {p44, p45};\n\tfma.rn.f32x2 %6, sb, q, %6;\n\t"
+      "mov.b64 q, {p46, p47};\n\tfma.rn.f32x2 %7, sb, q, %7;\n\t"
+      "mov.b64 q, {p48, p49};\n\tfma.rn.f32x2 %8, sb, q, %8;\n\t"
+      "mov.b64 q, {p50, p51};\n\tfma.rn.f32x2 %9, sb, q, %9;\n\t"
+      "mov.b64 q, {p52, p53};\n\tfma.rn.f32x2 %10, sb, q, %10;\n\t"
+      "mov.b64 q, {p54, p55};\n\tfma.rn.f32x2 %11, sb, q, %11;\n\t"
+      "mov.b64 q, {p56, p57};\n\tfma.rn.f32x2 %12, sb, q, %12;\n\t"
+      "mov.b64 q, {p58, p59};\n\tfma.rn.f32x2 %13, sb, q, %13;\n\t"
+      "mov.b64 q, {p60, p61};\n\tfma.rn.f32x2 %14, sb, q, %14;\n\t"
+      "mov.b64 q, {p62, p63};\n\tfma.rn.f32x2 %15, sb, q, %15;\n\t"
+      "}"
+      : "+l"(acc[0]), "+l"(acc[1]), "+l"(acc[2]), "+l"(acc[3]), "+l"(acc[4]),
+        "+l"(acc[5]), "+l"(acc[6]), "+l"(acc[7]), "+l"(acc[8]), "+l"(acc[9]),
+        "+l"(acc[10]), "+l"(acc[11]), "+l"(acc[12]), "+l"(acc[13]),
+        "+l"(acc[14]), "+l"(acc[15])
+      : "r"(taddr0), "r"(taddr1), "f"(s0), "f"(s1)
+      : "memory");
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -256,9 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
       int mb, nb;
       tile_coords(t, tiles_m, tiles_n, mb, nb);
-      float acc[32];
+      uint64_t acc[16];   // packed FP32 pairs: columns 2j, 2j+1
 #pragma unroll
-      for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < 16; ++j) acc[j] = 0;
       for (int ks = 0; ok && ks < nks; ++ks) {
         // Scale products of this stage (acquired through the stage's full
         // barrier), then let the stage go as far as this warp is concerned.
@@ -283,31 +342,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++s == STAGES) { s = 0; ph ^= 1u; }
         tc_fence_after();
         const uint32_t pbase = col0 + set * KPS * BN;
-        uint32_t r0[32], r1[32];
-        // K blocks 0 and 1 of the stage.
-        tmem_ld32_async(pbase, r0);
-        tmem_ld32_async(pbase + BN, r1);
-        tmem_ld_wait32(r0);
-        tmem_ld_wait32(r1);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          acc[j] = __fmaf_rn(sc.x, __uint_as_float(r0[j]), acc[j]);
-          acc[j] = __fmaf_rn(sc.y, __uint_as_float(r1[j]), acc[j]);
-        }
-        // K blocks 2 and 3; then the whole set is in registers.
-        tmem_ld32_async(pbase + 2 * BN, r0);
-        tmem_ld32_async(pbase + 3 * BN, r1);
-        tmem_ld_wait32(r0);
-        tmem_ld_wait32(r1);
+        // K blocks 0 and 1, then 2 and 3; after the second pair the whole
+        // set is in registers and goes back to the MMA warp.
+        promote_pair(acc, pbase, pbase + BN, sc.x, sc.y);
+        promote_pair(acc, pbase + 2 * BN, pbase + 3 * BN, sc.z, sc.w);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(pempty_bar(set));
         if (++set == NSETS) { set = 0; sph ^= 1u; }
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          acc[j] = __fmaf_rn(sc.z, __uint_as_float(r0[j]), acc[j]);
-          acc[j] = __fmaf_rn(sc.w, __uint_as_float(r1[j]), acc[j]);
-        }
       }
       if (!ok) break;
       // Epilogue: round to BF16 and store this thread's 32 columns.
@@ -318,7 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t w[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(
+              __uint_as_float(static_cast<uint32_t>(acc[j])),
+              __uint_as_float(static_cast<uint32_t>(acc[j] >> 32)));
           w[j] = *reinterpret_cast<const uint32_t *>(&b2);
         }
         if (a.c_vec16 && n + 32 <= a.N) {

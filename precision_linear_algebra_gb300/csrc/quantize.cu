@@ -25,7 +25,20 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kBlocksPerSm = 4;
-constexpr float kE4M3Max = 448.0f;
+
+// FP8 formats: 0 = E4M3 (max 448), 1 = E5M2 (max 57344).
+template <int FMT>
+struct Fp8Format;
+template <>
+struct Fp8Format<0> {
+  static constexpr float kMax = 448.0f;
+  static constexpr __nv_fp8_interpretation_t kKind = __NV_E4M3;
+};
+template <>
+struct Fp8Format<1> {
+  static constexpr float kMax = 57344.0f;
+  static constexpr __nv_fp8_interpretation_t kKind = __NV_E5M2;
+};
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -58,10 +71,11 @@ struct Scales {
   float qscale, scale;
 };
 
+template <int FMT = 0>
 __device__ __forceinline__ Scales scales_from_amax(float amax) {
   Scales s;
-  s.qscale = __fdiv_rn(kE4M3Max, amax);
-  s.scale = __fdiv_rn(amax, kE4M3Max);
+  s.qscale = __fdiv_rn(Fp8Format<FMT>::kMax, amax);
+  s.scale = __fdiv_rn(amax, Fp8Format<FMT>::kMax);
   if (amax == 0.0f || !isfinite(s.qscale)) {
     s.qscale = 1.0f;
     s.scale = 1.0f;
@@ -69,20 +83,23 @@ __device__ __forceinline__ Scales scales_from_amax(float amax) {
   return s;
 }
 
-// Two fp32 values -> two E4M3 codes (low byte = first value).
+// Two fp32 values -> two FP8 codes (low byte = first value).
+template <int FMT = 0>
 __device__ __forceinline__ uint32_t cvt2(float a, float b, float qs) {
   return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
       make_float2(__fmul_rn(a, qs), __fmul_rn(b, qs)), __NV_SATFINITE,
-      __NV_E4M3));
+      Fp8Format<FMT>::kKind));
 }
 
+template <int FMT = 0>
 __device__ __forceinline__ uint32_t cvt4(float4 v, float qs) {
-  return cvt2(v.x, v.y, qs) | (cvt2(v.z, v.w, qs) << 16);
+  return cvt2<FMT>(v.x, v.y, qs) | (cvt2<FMT>(v.z, v.w, qs) << 16);
 }
 
+template <int FMT = 0>
 __device__ __forceinline__ uint8_t cvt1(float a, float qs) {
-  return static_cast<uint8_t>(
-      __nv_cvt_float_to_fp8(__fmul_rn(a, qs), __NV_SATFINITE, __NV_E4M3));
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(
+      __fmul_rn(a, qs), __NV_SATFINITE, Fp8Format<FMT>::kKind));
 }
 
 __device__ __forceinline__ float4 ld_stream4(const float4 *p) {
@@ -134,12 +151,12 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // ------------------------------------------------------------------- cast
-template <int VEC>
+template <int VEC, int FMT>
 __global__ void __launch_bounds__(kThreads)
     cast_kernel(const float *__restrict__ x, int64_t rows, int64_t upr,
                 int64_t ldx, uint8_t *__restrict__ q, int64_t ldq,
                 bool contiguous, const float *amax_in, float *scale_out) {
-  const Scales s = scales_from_amax(*amax_in);
+  const Scales s = scales_from_amax<FMT>(*amax_in);
   if (blockIdx.x == 0 && threadIdx.x == 0) *scale_out = s.scale;
   const float qs = s.qscale;
   const int64_t n = rows * upr;
@@ -157,24 +174,24 @@ __global__ void __launch_bounds__(kThreads)
         const float4 b = ld_stream4(x4 + (last - i - stride));
         const float4 c = ld_stream4(x4 + (last - i - 2 * stride));
         const float4 d = ld_stream4(x4 + (last - i - 3 * stride));
-        q4[last - i] = cvt4(a, qs);
-        q4[last - i - stride] = cvt4(b, qs);
-        q4[last - i - 2 * stride] = cvt4(c, qs);
-        q4[last - i - 3 * stride] = cvt4(d, qs);
+        q4[last - i] = cvt4<FMT>(a, qs);
+        q4[last - i - stride] = cvt4<FMT>(b, qs);
+        q4[last - i - 2 * stride] = cvt4<FMT>(c, qs);
+        q4[last - i - 3 * stride] = cvt4<FMT>(d, qs);
       }
-      for (; i < n; i += stride) q4[last - i] = cvt4(ld_stream4(x4 + (last - i)), qs);
+      for (; i < n; i += stride) q4[last - i] = cvt4<FMT>(ld_stream4(x4 + (last - i)), qs);
     } else {
       for (; i < n; i += stride) {
         const int64_t r = i / upr, c = i - r * upr;
         const float4 v = ld_stream4(
             reinterpret_cast<const float4 *>(x + r * ldx + c * 4));
-        *reinterpret_cast<uint32_t *>(q + r * ldq + c * 4) = cvt4(v, qs);
+        *reinterpret_cast<uint32_t *>(q + r * ldq + c * 4) = cvt4<FMT>(v, qs);
       }
     }
   } else {
     for (; i < n; i += stride) {
       const int64_t r = i / upr, c = i - r * upr;
-      q[r * ldq + c] = cvt1(x[r * ldx + c], qs);
+      q[r * ldq + c] = cvt1<FMT>(x[r * ldx + c], qs);
     }
   }
 }
@@ -261,12 +278,14 @@ int grid_for(int64_t units, int threads) {
 
 using namespace fp8la;
 
-extern "C" fp8la_status fp8_quantize_pertensor(const float *x, int64_t rows,
-                                               int64_t cols, int64_t ldx,
-                                               uint8_t *q, int64_t ldq,
-                                               float *amax_out,
-                                               float *scale_out,
-                                               fp8la_stream_t stream) {
+namespace fp8la {
+namespace {
+
+template <int FMT>
+fp8la_status quantize_pertensor_impl(const float *x, int64_t rows,
+                                     int64_t cols, int64_t ldx, uint8_t *q,
+                                     int64_t ldq, float *amax_out,
+                                     float *scale_out, cudaStream_t s) {
   if (!amax_out || !scale_out || rows < 0 || cols < 0)
     return FP8LA_ERR_INVALID_ARG;
   const bool empty = rows == 0 || cols == 0;
@@ -275,12 +294,11 @@ extern "C" fp8la_status fp8_quantize_pertensor(const float *x, int64_t rows,
   if (rows > (int64_t(1) << 40) || cols > (int64_t(1) << 40))
     return FP8LA_ERR_UNSUPPORTED;
   if (sm_count() <= 0) return FP8LA_ERR_CUDA;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(amax_out, 0, sizeof(float), s) != cudaSuccess)
     return FP8LA_ERR_CUDA;
   if (empty) {
-    cast_kernel<1><<<1, 32, 0, s>>>(x, 0, 0, 0, q, 0, true, amax_out,
-                                    scale_out);
+    cast_kernel<1, FMT><<<1, 32, 0, s>>>(x, 0, 0, 0, q, 0, true, amax_out,
+                                         scale_out);
     return launch_status();
   }
   const bool vec4 = cols % 4 == 0 && ldx % 4 == 0 && ldq % 4 == 0 &&
@@ -292,16 +310,44 @@ extern "C" fp8la_status fp8_quantize_pertensor(const float *x, int64_t rows,
     const int g = grid_for(rows * upr, kThreads);
     amax_kernel<4><<<g, kThreads, 0, s>>>(x, rows, upr, ldx, contiguous,
                                           amax_out);
-    cast_kernel<4><<<g, kThreads, 0, s>>>(x, rows, upr, ldx, q, ldq,
-                                          contiguous, amax_out, scale_out);
+    cast_kernel<4, FMT><<<g, kThreads, 0, s>>>(x, rows, upr, ldx, q, ldq,
+                                               contiguous, amax_out, scale_out);
   } else {
     const int g = grid_for(rows * cols, kThreads);
     amax_kernel<1><<<g, kThreads, 0, s>>>(x, rows, cols, ldx, contiguous,
                                           amax_out);
-    cast_kernel<1><<<g, kThreads, 0, s>>>(x, rows, cols, ldx, q, ldq,
-                                          contiguous, amax_out, scale_out);
+    cast_kernel<1, FMT><<<g, kThreads, 0, s>>>(x, rows, cols, ldx, q, ldq,
+                                               contiguous, amax_out, scale_out);
   }
   return launch_status();
+}
+
+}  // namespace
+}  // namespace fp8la
+
+extern "C" fp8la_status fp8_quantize_pertensor(const float *x, int64_t rows,
+                                               int64_t cols, int64_t ldx,
+                                               uint8_t *q, int64_t ldq,
+                                               float *amax_out,
+                                               float *scale_out,
+                                               fp8la_stream_t stream) {
+  return quantize_pertensor_impl<0>(x, rows, cols, ldx, q, ldq, amax_out,
+                                    scale_out,
+                                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" fp8la_status fp8_quantize_pertensor_ex(
+    const float *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q,
+    int64_t ldq, float *amax_out, float *scale_out, int32_t format,
+    fp8la_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (format == FP8LA_FORMAT_E4M3)
+    return quantize_pertensor_impl<0>(x, rows, cols, ldx, q, ldq, amax_out,
+                                      scale_out, s);
+  if (format == FP8LA_FORMAT_E5M2)
+    return quantize_pertensor_impl<1>(x, rows, cols, ldx, q, ldq, amax_out,
+                                      scale_out, s);
+  return FP8LA_ERR_INVALID_ARG;
 }
 
 extern "C" fp8la_status fp8_quantize_blockwise_32x32(
