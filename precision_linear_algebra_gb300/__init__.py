@@ -163,6 +163,19 @@ def _ptr(t):
     return t.data_ptr() if t is not None else None
 
 
+def _ld(t):
+    """Leading dimension of a row-major 2-D tensor.  A single-row tensor's
+    row stride is meaningless (torch keeps whatever it was given, even 0), so
+    its row length is used."""
+    return t.stride(0) if t.shape[0] > 1 else max(t.shape[1], 1)
+
+
+def _ld_scales(t):
+    """As _ld, for a block-scale grid, whose row stride the GEMM reads by TMA
+    (a multiple of 4 floats even when there is one row)."""
+    return t.stride(0) if t.shape[0] > 1 else (t.shape[1] + 3) // 4 * 4
+
+
 def quantize_pertensor(x, q=None, amax=None, scale=None, fmt="e4m3"):
     """x: fp32 CUDA [rows][cols] (row stride may exceed cols).
 
@@ -176,7 +189,7 @@ def quantize_pertensor(x, q=None, amax=None, scale=None, fmt="e4m3"):
         q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
     amax = torch.empty(1, dtype=torch.float32, device=x.device) if amax is None else amax
     scale = torch.empty(1, dtype=torch.float32, device=x.device) if scale is None else scale
-    fp8_quantize_pertensor_ex(_ptr(x), rows, cols, x.stride(0), _ptr(q), q.stride(0),
+    fp8_quantize_pertensor_ex(_ptr(x), rows, cols, _ld(x), _ptr(q), _ld(q),
                               _ptr(amax), _ptr(scale), _FORMATS[fmt], _stream())
     return q, amax, scale
 
@@ -194,8 +207,8 @@ def quantize_blockwise_32x32(x, q=None, scales=None):
         tc = (cols + 31) // 32
         scales = torch.empty(((rows + 31) // 32, (tc + 3) // 4 * 4),
                              dtype=torch.float32, device=x.device)[:, :tc]
-    fp8_quantize_blockwise_32x32(_ptr(x), rows, cols, x.stride(0), _ptr(q), q.stride(0),
-                                 _ptr(scales), scales.stride(0), _stream())
+    fp8_quantize_blockwise_32x32(_ptr(x), rows, cols, _ld(x), _ptr(q), _ld(q),
+                                 _ptr(scales), _ld(scales), _stream())
     return q, scales
 
 
@@ -209,10 +222,10 @@ def gemm(A, B, scale_a, scale_b, C=None, a_fmt="e4m3", b_fmt="e4m3"):
     if C is None:
         C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     if a_fmt == "e4m3" and b_fmt == "e4m3":
-        fp8_gemm(_ptr(A), A.stride(0), _ptr(B), B.stride(0), _ptr(C), C.stride(0),
+        fp8_gemm(_ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C),
                  M, N, K, _ptr(scale_a), _ptr(scale_b), _stream())
     else:
-        fp8_gemm_ex(_ptr(A), A.stride(0), _ptr(B), B.stride(0), _ptr(C), C.stride(0),
+        fp8_gemm_ex(_ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C),
                     M, N, K, _ptr(scale_a), _ptr(scale_b), _FORMATS[a_fmt],
                     _FORMATS[b_fmt], _stream())
     return C
@@ -225,9 +238,9 @@ def gemm_blockscaled_32x32(A, B, sa, sb, C=None):
     N = B.shape[0]
     if C is None:
         C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
-    fp8_gemm_blockscaled_32x32(_ptr(A), A.stride(0), _ptr(B), B.stride(0), _ptr(C),
-                               C.stride(0), M, N, K, _ptr(sa), sa.stride(0),
-                               _ptr(sb), sb.stride(0), _stream())
+    fp8_gemm_blockscaled_32x32(_ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C),
+                               _ld(C), M, N, K, _ptr(sa), _ld_scales(sa),
+                               _ptr(sb), _ld_scales(sb), _stream())
     return C
 
 
@@ -239,8 +252,8 @@ def grouped_gemm(m_offsets, A, B, scale_a, scale_b, C=None):
     N = B.shape[1]
     if C is None:
         C = torch.empty((cap, N), dtype=torch.bfloat16, device=A.device)
-    fp8_grouped_gemm(E, _ptr(m_offsets), cap, _ptr(A), A.stride(0), _ptr(B),
-                     B.stride(1), B.stride(0), _ptr(C), C.stride(0), N, K,
+    fp8_grouped_gemm(E, _ptr(m_offsets), cap, _ptr(A), _ld(A), _ptr(B),
+                     B.stride(1) if N > 1 else K, B.stride(0), _ptr(C), _ld(C), N, K,
                      _ptr(scale_a), _ptr(scale_b), _stream())
     return C
 
