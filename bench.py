@@ -319,7 +319,73 @@ def _workload_pertensor(fl, torch, dev, sptr, ph):
         main.wait_stream(sq)
         main.wait_stream(sg)
 
-    return dict(step=step, pipeline=(pbegin, pstep, pend), flops=FLOPS, launches=5,
+    # Pipelined end to end: step i's fp32 inputs come from pinned host memory
+    # (A and B on two copy streams), its C goes back to a pinned host buffer
+    # on a third; host->device copies of step i+1, compute of step i and the
+    # device->host copy of step i-1 overlap.  Device inputs and host outputs
+    # are double-buffered; events keep every buffer from being overwritten
+    # while still in use.
+    e2e = {}
+
+    def ebegin(A_h, B_h, C_h2):
+        if not e2e:
+            e2e.update(A=[A, torch.empty_like(A)], B=[B, torch.empty_like(B)],
+                       C=[C, torch.empty_like(C)],
+                       sa=torch.cuda.Stream(dev), sb=torch.cuda.Stream(dev),
+                       so=torch.cuda.Stream(dev),
+                       loaded=[torch.cuda.Event(), torch.cuda.Event()],
+                       quantized=[torch.cuda.Event(), torch.cuda.Event()],
+                       computed=[torch.cuda.Event(), torch.cuda.Event()],
+                       stored=[torch.cuda.Event(), torch.cuda.Event()])
+        e2e.update(A_h=A_h, B_h=B_h, C_h=C_h2)
+        for k in ("loaded", "quantized", "computed", "stored"):
+            for ev in e2e[k]:
+                ev.record(main)
+        for st in (e2e["sa"], e2e["sb"], e2e["so"], sq, sg):
+            st.wait_stream(main)
+
+    def estep(i):
+        b = i & 1
+        E = e2e
+        # inputs: buffer b is free once quantize(i-2) has read it
+        E["sa"].wait_event(E["quantized"][b])
+        E["sb"].wait_event(E["quantized"][b])
+        with torch.cuda.stream(E["sa"]):
+            E["A"][b].copy_(E["A_h"], non_blocking=True)
+        with torch.cuda.stream(E["sb"]):
+            E["B"][b].copy_(E["B_h"], non_blocking=True)
+        ev_a, ev_b = torch.cuda.Event(), torch.cuda.Event()
+        ev_a.record(E["sa"])
+        ev_b.record(E["sb"])
+        # quantize (codes double-buffered as in the device-resident pipeline)
+        sq.wait_event(ev_a)
+        sq.wait_event(ev_b)
+        sq.wait_event(gdone[b])
+        fl.fp8_quantize_pertensor(P(E["A"][b]), N_SIZE, N_SIZE, N_SIZE, P(qa2[b]), N_SIZE,
+                                  P(amax2, 2 * b), P(scale2, 2 * b), sq.cuda_stream)
+        fl.fp8_quantize_pertensor(P(E["B"][b]), N_SIZE, N_SIZE, N_SIZE, P(qb2[b]), N_SIZE,
+                                  P(amax2, 2 * b + 1), P(scale2, 2 * b + 1), sq.cuda_stream)
+        E["quantized"][b].record(sq)
+        qdone[b].record(sq)
+        # GEMM into C[b] once the D2H of step i-2 has drained it
+        sg.wait_event(qdone[b])
+        sg.wait_event(E["stored"][b])
+        fl.fp8_gemm(P(qa2[b]), N_SIZE, P(qb2[b]), N_SIZE, P(E["C"][b]), N_SIZE, N_SIZE,
+                    N_SIZE, N_SIZE, P(scale2, 2 * b), P(scale2, 2 * b + 1), sg.cuda_stream)
+        gdone[b].record(sg)
+        E["computed"][b].record(sg)
+        # result back to the host
+        E["so"].wait_event(E["computed"][b])
+        with torch.cuda.stream(E["so"]):
+            E["C_h"][b].copy_(E["C"][b], non_blocking=True)
+        E["stored"][b].record(E["so"])
+
+    def eend():
+        for st in (e2e["sa"], e2e["sb"], e2e["so"], sq, sg):
+            main.wait_stream(st)
+
+    return dict(step=step, pipeline=(pbegin, pstep, pend), e2e_pipeline=(ebegin, estep, eend),
+                flops=FLOPS, launches=5,
                 workload=WORKLOAD,
                 config={"M": N_SIZE, "N": N_SIZE, "K": N_SIZE,
                         "l2": "inputs 2 x 268 MB fp32 > 129 MB L2; no flush"},
@@ -525,6 +591,7 @@ def run_gpu(args):
     hosts = [(d, torch.from_numpy(h).pin_memory()) for d, h in W["inputs"]]
     outs = [(o, torch.empty(o.shape, dtype=o.dtype).pin_memory()) for o in W["outputs"]]
     e2e_steps = max(3, min(args.steps, 30))
+    e2e_pipelined = args.schedule == "pipelined" and "e2e_pipeline" in W
 
     def e2e_step():
         for d, h in hosts:
@@ -533,16 +600,43 @@ def run_gpu(args):
         for o, h in outs:
             h.copy_(o, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    e2e_serial_ms = None
+    if e2e_pipelined:
+        ebegin, estep, eend = W["e2e_pipeline"]
+        C_h2 = [outs[0][1], torch.empty_like(outs[0][1]).pin_memory()]
+        # serial reference first
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_serial_ms = e0.elapsed_time(e1) / e2e_steps
+        ebegin(hosts[0][1], hosts[1][1], C_h2)
+        for i in range(3):
+            estep(i)
+        eend()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        ebegin(hosts[0][1], hosts[1][1], C_h2)
+        for i in range(e2e_steps):
+            estep(i)
+        eend()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    else:
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     if world > 1:
         e2e_ms = max_over_ranks(e2e_ms, dev)
@@ -588,7 +682,9 @@ def run_gpu(args):
                                            if pipelined else value)},
             "e2e": {"value": world * W["flops"] / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms},
+                    "ms_per_step": e2e_ms,
+                    "schedule": "pipelined" if e2e_pipelined else "serial",
+                    "serial_ms_per_step": e2e_serial_ms if e2e_pipelined else e2e_ms},
             "gpu_launches": W["launches"] * args.steps * (len(args.linears.split(",")) / 4.0
                                                            if args.workload == "blockscaled"
                                                            and args.linears else 1),

@@ -130,44 +130,44 @@ __device__ __forceinline__ void promote_pair(uint64_t (&acc)[16],
   asm volatile(
       "{\n\t"
       ".reg .b32 p<64>;\n\t"
-      ".reg .b64 q, sa, sb;\n\t"
+      ".reg .b64 q<32>, sa, sb;\n\t"
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {p0, p1, p2, p3, p4, p5, p6, p7, p8, p9, p10, p11, p12, p13, p14, p15, p16, p17, p18, p19, p20, p21, p22, p23, p24, p25, p26, p27, p28, p29, p30, p31}, [%16];\n\t"
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {p32, p33, p34, p35, p36, p37, p38, p39, p40, p41, p42, p43, p44, p45, p46, p47, p48, p49, p50, p51, p52, p53, p54, p55, p56, p57, p58, p59, p60, p61, p62, p63}, [%17];\n\t"
       "tcgen05.wait::ld.sync.aligned;\n\t"
       "mov.b64 sa, {%18, %18};\n\t"
       "mov.b64 sb, {%19, %19};\n\t"
-      "mov.b64 q, {p0, p1};\n\tfma.rn.f32x2 %0, sa, q, %0;\n\t"
-      "mov.b64 q, {p2, p3};\n\tfma.rn.f32x2 %1, sa, q, %1;\n\t"
-      "mov.b64 q, {p4, p5};\n\tfma.rn.f32x2 %2, sa, q, %2;\n\t"
-      "mov.b64 q, {p6, p7};\n\tfma.rn.f32x2 %3, sa, q, %3;\n\t"
-      "mov.b64 q, {p8, p9};\n\tfma.rn.f32x2 %4, sa, q, %4;\n\t"
-      "mov.b64 q, {p10, p11};\n\tfma.rn.f32x2 %5, sa, q, %5;\n\t"
-      "mov.b64 q, {p12, p13};\n\tfma.rn.f32x2 %6, sa, q, %6;\n\t"
-      "mov.b64 q, {p14, p15};\n\tfma.rn.f32x2 %7, sa, q, %7;\n\t"
-      "mov.b64 q, {p16, p17};\n\tfma.rn.f32x2 %8, sa, q, %8;\n\t"
-      "mov.b64 q, {p18, p19};\n\tfma.rn.f32x2 %9, sa, q, %9;\n\t"
-      "mov.b64 q, {p20, p21};\n\tfma.rn.f32x2 %10, sa, q, %10;\n\t"
-      "mov.b64 q, {p22, p23};\n\tfma.rn.f32x2 %11, sa, q, %11;\n\t"
-      "mov.b64 q, {p24, p25};\n\tfma.rn.f32x2 %12, sa, q, %12;\n\t"
-      "mov.b64 q, {p26, p27};\n\tfma.rn.f32x2 %13, sa, q, %13;\n\t"
-      "mov.b64 q, {p28, p29};\n\tfma.rn.f32x2 %14, sa, q, %14;\n\t"
-      "mov.b64 q, {p30, p31};\n\tfma.rn.f32x2 %15, sa, q, %15;\n\t"
-      "mov.b64 q, {p32, p33};\n\tfma.rn.f32x2 %0, sb, q, %0;\n\t"
-      "mov.b64 q, {p34, p35};\n\tfma.rn.f32x2 %1, sb, q, %1;\n\t"
-      "mov.b64 q, {p36, p37};\n\tfma.rn.f32x2 %2, sb, q, %2;\n\t"
-      "mov.b64 q, {p38, p39};\n\tfma.rn.f32x2 %3, sb, q, %3;\n\t"
-      "mov.b64 q, {p40, p41};\n\tfma.rn.f32x2 %4, sb, q, %4;\n\t"
-      "mov.b64 q, {p42, p43};\n\tfma.rn.f32x2 %5, sb, q, %5;\n\t"
-      "mov.b64 q, {p44, p45};\n\tfma.rn.f32x2 %6, sb, q, %6;\n\t"
-      "mov.b64 q, {p46, p47};\n\tfma.rn.f32x2 %7, sb, q, %7;\n\t"
-      "mov.b64 q, {p48, p49};\n\tfma.rn.f32x2 %8, sb, q, %8;\n\t"
-      "mov.b64 q, {p50, p51};\n\tfma.rn.f32x2 %9, sb, q, %9;\n\t"
-      "mov.b64 q, {p52, p53};\n\tfma.rn.f32x2 %10, sb, q, %10;\n\t"
-      "mov.b64 q, {p54, p55};\n\tfma.rn.f32x2 %11, sb, q, %11;\n\t"
-      "mov.b64 q, {p56, p57};\n\tfma.rn.f32x2 %12, sb, q, %12;\n\t"
-      "mov.b64 q, {p58, p59};\n\tfma.rn.f32x2 %13, sb, q, %13;\n\t"
-      "mov.b64 q, {p60, p61};\n\tfma.rn.f32x2 %14, sb, q, %14;\n\t"
-      "mov.b64 q, {p62, p63};\n\tfma.rn.f32x2 %15, sb, q, %15;\n\t"
+      "mov.b64 q0, {p0, p1};\n\tfma.rn.f32x2 %0, sa, q0, %0;\n\t"
+      "mov.b64 q1, {p2, p3};\n\tfma.rn.f32x2 %1, sa, q1, %1;\n\t"
+      "mov.b64 q2, {p4, p5};\n\tfma.rn.f32x2 %2, sa, q2, %2;\n\t"
+      "mov.b64 q3, {p6, p7};\n\tfma.rn.f32x2 %3, sa, q3, %3;\n\t"
+      "mov.b64 q4, {p8, p9};\n\tfma.rn.f32x2 %4, sa, q4, %4;\n\t"
+      "mov.b64 q5, {p10, p11};\n\tfma.rn.f32x2 %5, sa, q5, %5;\n\t"
+      "mov.b64 q6, {p12, p13};\n\tfma.rn.f32x2 %6, sa, q6, %6;\n\t"
+      "mov.b64 q7, {p14, p15};\n\tfma.rn.f32x2 %7, sa, q7, %7;\n\t"
+      "mov.b64 q8, {p16, p17};\n\tfma.rn.f32x2 %8, sa, q8, %8;\n\t"
+      "mov.b64 q9, {p18, p19};\n\tfma.rn.f32x2 %9, sa, q9, %9;\n\t"
+      "mov.b64 q10, {p20, p21};\n\tfma.rn.f32x2 %10, sa, q10, %10;\n\t"
+      "mov.b64 q11, {p22, p23};\n\tfma.rn.f32x2 %11, sa, q11, %11;\n\t"
+      "mov.b64 q12, {p24, p25};\n\tfma.rn.f32x2 %12, sa, q12, %12;\n\t"
+      "mov.b64 q13, {p26, p27};\n\tfma.rn.f32x2 %13, sa, q13, %13;\n\t"
+      "mov.b64 q14, {p28, p29};\n\tfma.rn.f32x2 %14, sa, q14, %14;\n\t"
+      "mov.b64 q15, {p30, p31};\n\tfma.rn.f32x2 %15, sa, q15, %15;\n\t"
+      "mov.b64 q16, {p32, p33};\n\tfma.rn.f32x2 %0, sb, q16, %0;\n\t"
+      "mov.b64 q17, {p34, p35};\n\tfma.rn.f32x2 %1, sb, q17, %1;\n\t"
+      "mov.b64 q18, {p36, p37};\n\tfma.rn.f32x2 %2, sb, q18, %2;\n\t"
+      "mov.b64 q19, {p38, p39};\n\tfma.rn.f32x2 %3, sb, q19, %3;\n\t"
+      "mov.b64 q20, {p40, p41};\n\tfma.rn.f32x2 %4, sb, q20, %4;\n\t"
+      "mov.b64 q21, {p42, p43};\n\tfma.rn.f32x2 %5, sb, q21, %5;\n\t"
+      "mov.b64 q22, {p44, p45};\n\tfma.rn.f32x2 %6, sb, q22, %6;\n\t"
+      "mov.b64 q23, {p46, p47};\n\tfma.rn.f32x2 %7, sb, q23, %7;\n\t"
+      "mov.b64 q24, {p48, p49};\n\tfma.rn.f32x2 %8, sb, q24, %8;\n\t"
+      "mov.b64 q25, {p50, p51};\n\tfma.rn.f32x2 %9, sb, q25, %9;\n\t"
+      "mov.b64 q26, {p52, p53};\n\tfma.rn.f32x2 %10, sb, q26, %10;\n\t"
+      "mov.b64 q27, {p54, p55};\n\tfma.rn.f32x2 %11, sb, q27, %11;\n\t"
+      "mov.b64 q28, {p56, p57};\n\tfma.rn.f32x2 %12, sb, q28, %12;\n\t"
+      "mov.b64 q29, {p58, p59};\n\tfma.rn.f32x2 %13, sb, q29, %13;\n\t"
+      "mov.b64 q30, {p60, p61};\n\tfma.rn.f32x2 %14, sb, q30, %14;\n\t"
+      "mov.b64 q31, {p62, p63};\n\tfma.rn.f32x2 %15, sb, q31, %15;\n\t"
       "}"
       : "+l"(acc[0]), "+l"(acc[1]), "+l"(acc[2]), "+l"(acc[3]), "+l"(acc[4]),
         "+l"(acc[5]), "+l"(acc[6]), "+l"(acc[7]), "+l"(acc[8]), "+l"(acc[9]),
