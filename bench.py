@@ -395,6 +395,64 @@ def _workload_pertensor(fl, torch, dev, sptr, ph):
                 qprofile=("quantize_pertensor_8192", QUANT_SOURCES))
 
 
+def _workload_square(n):
+    """Per-tensor quantize(A), quantize(B) + GEMM at M = N = K = n (N(0,1)
+    inputs).  These sizes are launch-bound, so the timed step replays one
+    CUDA graph holding the step's five launches."""
+
+    def build(fl, torch, dev, sptr, ph):
+        from precision_linear_algebra_gb300 import workloads
+        A_np, B_np = workloads.square(n, seed=0)
+        A = torch.from_numpy(A_np).to(dev)
+        B = torch.from_numpy(B_np).to(dev)
+        qa = torch.empty((n, n), dtype=torch.uint8, device=dev)
+        qb = torch.empty_like(qa)
+        amax = torch.empty(2, dtype=torch.float32, device=dev)
+        scale = torch.empty(2, dtype=torch.float32, device=dev)
+        C = torch.empty((n, n), dtype=torch.bfloat16, device=dev)
+        P = lambda t, i=0: t.data_ptr() + i * t.element_size()
+
+        def launches(stream_ptr):
+            fl.fp8_quantize_pertensor(P(A), n, n, n, P(qa), n, P(amax, 0), P(scale, 0),
+                                      stream_ptr)
+            fl.fp8_quantize_pertensor(P(B), n, n, n, P(qb), n, P(amax, 1), P(scale, 1),
+                                      stream_ptr)
+            fl.fp8_gemm(P(qa), n, P(qb), n, P(C), n, n, n, n, P(scale, 0), P(scale, 1),
+                        stream_ptr)
+
+        def step():
+            ph.mark("quant")
+            fl.fp8_quantize_pertensor(P(A), n, n, n, P(qa), n, P(amax, 0), P(scale, 0), sptr)
+            fl.fp8_quantize_pertensor(P(B), n, n, n, P(qb), n, P(amax, 1), P(scale, 1), sptr)
+            ph.mark("quant")
+            ph.mark("gemm")
+            fl.fp8_gemm(P(qa), n, P(qb), n, P(C), n, n, n, n, P(scale, 0), P(scale, 1), sptr)
+            ph.mark("gemm")
+
+        # One step captured as a CUDA graph (after a warm-up on a side stream,
+        # so that one-time library set-up happens outside the capture).
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cap):
+            launches(cap.cuda_stream)
+        torch.cuda.current_stream(dev).wait_stream(cap)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            launches(cap.cuda_stream)
+        torch.cuda.synchronize()
+        return dict(step=step, graph=graph, flops=2.0 * n ** 3, launches=5,
+                    workload=("per-tensor E4M3 quantize(A), quantize(B) + scaled GEMM, "
+                              "M=N=K=%d, A, B ~ N(0,1), seed 0; one CUDA graph per step" % n),
+                    config={"M": n, "N": n, "K": n,
+                            "l2": "L2-resident inputs (%d KB fp32); no flush" % (8 * n * n // 1024)},
+                    inputs=[(A, A_np), (B, B_np)], outputs=[C], quant_elems=2 * n * n,
+                    gemm_label="gemm_e4m3_pair_kernel<false>", gemm_bytes=4 * n * n,
+                    profile=("gemm_e4m3_square_%d" % n, GEMM_SOURCES),
+                    qprofile=("quantize_square_%d" % n, QUANT_SOURCES))
+    return build
+
+
 def _workload_blockscaled(fl, torch, dev, sptr, ph, linears=("qkv", "attn_out", "gate_up", "down")):
     from precision_linear_algebra_gb300 import workloads
     items = []
@@ -492,7 +550,8 @@ def _workload_grouped(fl, torch, dev, sptr, ph):
 
 
 WORKLOADS = {"pertensor8192": _workload_pertensor, "blockscaled": _workload_blockscaled,
-             "grouped": _workload_grouped}
+             "grouped": _workload_grouped, "square256": _workload_square(256),
+             "square1024": _workload_square(1024)}
 
 
 def run_gpu(args):
@@ -562,10 +621,14 @@ def run_gpu(args):
             pstep(i)
         pend()
         torch.cuda.synchronize()
+    graph = W.get("graph")
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    if pipelined:
+    if graph is not None:
+        for _ in range(args.steps):
+            graph.replay()
+    elif pipelined:
         pbegin()
         for i in range(args.steps):
             pstep(i)
@@ -676,7 +739,8 @@ def run_gpu(args):
                                       5 if args.workload == "blockscaled" else QUANT_BYTES_PER_ELEM},
             "breakdown": {"gemm_ms": g_avg, "quantize_ms": q_avg,
                           "gemm_tflops": gemm_tflops, "quantize_gbs": quant_gbs,
-                          "schedule": "pipelined" if pipelined else "serial",
+                          "schedule": ("cuda graph" if graph is not None else
+                                       "pipelined" if pipelined else "serial"),
                           "serial_ms_per_step": serial_ms if pipelined else ms_step,
                           "serial_value": (world * W["flops"] / (serial_ms * 1e-3) / 1e12
                                            if pipelined else value)},

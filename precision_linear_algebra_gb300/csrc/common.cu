@@ -57,6 +57,31 @@ unsigned *status_word_ptr() {
 
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(); }
 
+int current_device_index() { return current_device(); }
+
+namespace {
+std::atomic<bool> g_setup[detail::kSlots][detail::kDevs];
+std::atomic<int> g_clusters[detail::kSlots][detail::kDevs];
+}  // namespace
+
+namespace detail {
+bool setup_done(int slot, int dev) { return g_setup[slot][dev].load(); }
+void mark_setup_done(int slot, int dev) { g_setup[slot][dev].store(true); }
+}  // namespace detail
+
+int cached_clusters(int slot) {
+  const int dev = current_device();
+  if (dev < 0 || slot < 0 || slot >= detail::kSlots) return -1;
+  const int v = g_clusters[slot][dev].load();
+  return v > 0 ? v : -1;
+}
+
+void cache_clusters(int slot, int clusters) {
+  const int dev = current_device();
+  if (dev < 0 || slot < 0 || slot >= detail::kSlots) return;
+  g_clusters[slot][dev].store(clusters);
+}
+
 int sm_count() {
   const int dev = current_device();
   if (dev < 0) return -1;

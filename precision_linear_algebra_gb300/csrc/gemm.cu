@@ -674,8 +674,10 @@ fp8la_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB,
                          cudaStream_t s) {
   using L = Smem<kBN, kStages>;
   auto kern = gemm_e4m3_kernel<kBN, kStages, GROUPED>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           L::kAlloc) != cudaSuccess)
+  if (once_per_device(GROUPED ? 1 : 0, [&] {
+        return cudaFuncSetAttribute(
+            kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+      }) != cudaSuccess)
     return FP8LA_ERR_CUDA;
   const int sms = sm_count();
   if (sms <= 0) return FP8LA_ERR_CUDA;
@@ -693,8 +695,11 @@ fp8la_status launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB,
                               cudaStream_t s) {
   using L = PairSmem;
   auto kern = gemm_e4m3_pair_kernel<GROUPED>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           L::kAlloc) != cudaSuccess)
+  const int slot = GROUPED ? 3 : 2;
+  if (once_per_device(slot, [&] {
+        return cudaFuncSetAttribute(
+            kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+      }) != cudaSuccess)
     return FP8LA_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -708,10 +713,13 @@ fp8la_status launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(2, 1, 1);
-  int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess ||
-      clusters < 1)
-    return FP8LA_ERR_CUDA;
+  int clusters = cached_clusters(slot);
+  if (clusters < 1) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess ||
+        clusters < 1)
+      return FP8LA_ERR_CUDA;
+    cache_clusters(slot, clusters);
+  }
   int64_t n = max_tiles < clusters ? max_tiles : clusters;
   if (n < 1) n = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * n), 1, 1);

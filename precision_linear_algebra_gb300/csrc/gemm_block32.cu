@@ -485,9 +485,11 @@ extern "C" fp8la_status fp8_gemm_blockscaled_32x32(
   args.status = status;
   args.timeout_ns = wait_timeout_ns();
   args.c_vec16 = aligned16(C) && ldc % 8 == 0;
-  if (cudaFuncSetAttribute(gemm_e4m3_block32_kernel,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Lay::kAlloc) != cudaSuccess)
+  if (once_per_device(4, [] {
+        return cudaFuncSetAttribute(gemm_e4m3_block32_kernel,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Lay::kAlloc);
+      }) != cudaSuccess)
     return FP8LA_ERR_CUDA;
   const int sms = sm_count();
   if (sms <= 0) return FP8LA_ERR_CUDA;

@@ -31,12 +31,44 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType,
                                    CUtensorMapFloatOOBfill);
 EncodeTiledFn encode_tiled_fn();
 
+// Index of the current device, or -1.
+int current_device_index();
+
+// Per-device once-only set-up of a kernel: runs `fn` (returning a
+// cudaError_t) the first time it is called for (slot, device) and caches a
+// success; later calls return cudaSuccess without touching the runtime, so
+// that a call sequence can be captured into a CUDA graph.  `slot` names the
+// kernel (a small integer per kernel instantiation).
+template <typename F>
+cudaError_t once_per_device(int slot, F &&fn);
+
+// Cached cudaOccupancyMaxActiveClusters result for (slot, device), or -1.
+int cached_clusters(int slot);
+void cache_clusters(int slot, int clusters);
+
 inline bool aligned16(const void *p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
 
 inline fp8la_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? FP8LA_OK : FP8LA_ERR_CUDA;
+}
+
+namespace detail {
+constexpr int kSlots = 16;
+constexpr int kDevs = 64;
+bool setup_done(int slot, int dev);
+void mark_setup_done(int slot, int dev);
+}  // namespace detail
+
+template <typename F>
+cudaError_t once_per_device(int slot, F &&fn) {
+  const int dev = current_device_index();
+  if (dev < 0 || slot < 0 || slot >= detail::kSlots) return fn();
+  if (detail::setup_done(slot, dev)) return cudaSuccess;
+  const cudaError_t e = fn();
+  if (e == cudaSuccess) detail::mark_setup_done(slot, dev);
+  return e;
 }
 
 }  // namespace fp8la

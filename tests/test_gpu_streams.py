@@ -66,3 +66,49 @@ def test_two_stream_pipeline_matches_serial():
         assert torch.equal(outs[i].view(torch.int16), ref[i].view(torch.int16)), i
     # the steps really differ from each other
     assert not torch.equal(ref[0], ref[1])
+
+
+def test_cuda_graph_capture_and_replay():
+    """A quantize -> quantize -> GEMM step captured into a CUDA graph and
+    replayed gives the eager result; replays see updated inputs."""
+    import torch
+    fl = lib()
+    n = 512
+    A_np, B_np = workloads.square(n, seed=4)
+    A, B = to_dev(A_np), to_dev(B_np)
+    qa = torch.empty((n, n), dtype=torch.uint8, device="cuda")
+    qb = torch.empty_like(qa)
+    amax = torch.empty(2, dtype=torch.float32, device="cuda")
+    scale = torch.empty(2, dtype=torch.float32, device="cuda")
+    C = torch.empty((n, n), dtype=torch.bfloat16, device="cuda")
+    P = lambda t, i=0: t.data_ptr() + i * t.element_size()
+
+    def launches(s):
+        fl.fp8_quantize_pertensor(P(A), n, n, n, P(qa), n, P(amax, 0), P(scale, 0), s)
+        fl.fp8_quantize_pertensor(P(B), n, n, n, P(qb), n, P(amax, 1), P(scale, 1), s)
+        fl.fp8_gemm(P(qa), n, P(qb), n, P(C), n, n, n, n, P(scale, 0), P(scale, 1), s)
+
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        launches(cap.cuda_stream)            # eager warm-up: one-time set-up
+    torch.cuda.current_stream().wait_stream(cap)
+    torch.cuda.synchronize()
+    eager = C.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        launches(cap.cuda_stream)
+    C.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(C.view(torch.int16), eager.view(torch.int16))
+    # new inputs through the same graph
+    A.mul_(3.0)
+    B.mul_(0.5)
+    g.replay()
+    torch.cuda.synchronize()
+    ref_qa, _, _ = fl.quantize_pertensor(A)
+    ref_qb, _, _ = fl.quantize_pertensor(B)
+    torch.cuda.synchronize()
+    assert torch.equal(qa, ref_qa) and torch.equal(qb, ref_qb)
+    assert fl.device_status() == 0
