@@ -15,32 +15,32 @@
 // by one tcgen05.mma (M=128, N=128, K=32) into a fresh TMEM buffer and then
 // weighted and added on the CUDA cores.
 //
-// Design (one CTA per SM, persistent, 18 warps).  The promotion costs one
+// Design (one CTA per SM, persistent, 10 warps).  The promotion costs one
 // FP32 FMA per output per 32-wide K block, against 32 tensor-core FMAs: on
 // 128 FP32 lanes per SM versus 8192 tensor FMAs per clock this caps the
 // kernel near half the dense FP8 peak, so the design keeps the FMA pipe
 // busy and puts all synchronisation at the granularity of 128-wide K stages:
-//   * warp 16: producer (lane 0).  Per 128-wide K stage (8-stage ring) it
+//   * warp 8: producer (lane 0).  Per 128-wide K stage (8-stage ring) it
 //     issues four TMA loads on one barrier: a 128 x 128 A tile, a 64 x 128 B
 //     tile, and the stage's scale boxes sa[4 row tiles][4 K blocks] and
 //     sb[2 column tiles][4 K blocks].  Nothing on the producer waits for
 //     global memory, so it runs up to eight stages ahead.
-//   * warp 17: MMA issuer (lane 0).  Per stage, four MMAs (M=128, N=64, K=32,
+//   * warp 9: MMA issuer (lane 0).  Per stage, four MMAs (M=128, N=64, K=32,
 //     one per 32-wide K block) into the four 64-column TMEM partial buffers
 //     of one of two buffer sets; one commit hands the whole set over.
-//   * warps 0-15: promotion, four per SM sub-partition so that they hide each
-//     other's TMEM-load latency.  Warp w reads TMEM lanes 32(w%4).. (C rows)
-//     and columns 16(w/4)..+15 of each partial, inside one 32 x 32 scale
-//     tile, so its scale is one number per K block: sa * sb from two 16-byte
+//   * warps 0-7: promotion.  Warp w reads TMEM lanes 32(w%4).. (C rows) and
+//     columns 32(w/4)..+31 of each partial, exactly one 32 x 32 scale tile,
+//     so its scale is one number per K block: sa * sb from two 16-byte
 //     shared-memory vectors per stage.  Each thread keeps its row's 32 FP32 accumulators in
-//     registers (as 16 packed pairs) and adds (sa*sb) * partial with packed
-//     FMAs (fma.rn.f32x2), two K blocks' partials per TMEM wait, each pair
-//     of K blocks in one asm statement.  After the last stage of a tile it
-//     rounds to BF16 and stores 32 bytes.
-//   * A stage is recycled only when its MMAs have completed and all sixteen
-//     promotion warps have read its scales (empty count 1 + 16); a
-//     partial-buffer set is reused once all sixteen warps hold its data in
-//     registers (pempty count 16).
+//     registers and adds (sa*sb) * partial with scalar FP32 FMAs, two K
+//     blocks' partials per TMEM wait, each pair of K blocks in one asm
+//     statement (packed f32x2 FMAs would need the loaded registers moved
+//     into pairs first, costing more issue slots than they save).  After the last stage of a tile it
+//     rounds to BF16 and stores 64 bytes.
+//   * A stage is recycled only when its MMAs have completed and all eight
+//     promotion warps have read its scales (empty count 1 + 8); a
+//     partial-buffer set is reused once all eight warps hold its data in
+//     registers (pempty count 8).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -56,10 +56,10 @@ constexpr int KB = 32;           // scale block along K, = K per MMA
 constexpr int KPS = BK / KB;     // K blocks per stage (4)
 constexpr int STAGES = 8;
 constexpr int NSETS = 2;         // TMEM partial-buffer sets, KPS buffers each
-constexpr int kPromoWarps = 16;
-constexpr int kProducerWarp = 16;
-constexpr int kMmaWarp = 17;
-constexpr int kThreads = 576;
+constexpr int kPromoWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
 constexpr int GROUP_M = 16;
 constexpr int kTmemCols = NSETS * KPS * BN;  // 512
 
@@ -120,42 +120,92 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n,
   nb = r / gm;
 }
 
-// Promotion of two K blocks' partials, 16 columns of one lane row each:
+// Promotion of two K blocks' partials, 32 columns of one lane row each:
 // loads both from TMEM, waits, and adds s0 * first + s1 * second into the
-// 16 FP32 accumulators held as 8 packed pairs (acc[j] = columns 2j, 2j+1),
-// with packed FMAs fma.rn.f32x2 (each lane of a pair rounded once).  One
-// asm statement, so the loaded values never leave it.
-__device__ __forceinline__ void promote_pair16(uint64_t (&acc)[8],
-                                               uint32_t taddr0, uint32_t taddr1,
-                                               float s0, float s1) {
+// thread's 32 FP32 accumulators with scalar FMAs (fma.rn.f32, one rounding
+// each).  One asm statement, so the loaded values never leave it.
+__device__ __forceinline__ void promote_pair(float (&acc)[32], uint32_t taddr0,
+                                             uint32_t taddr1, float s0,
+                                             float s1) {
   asm volatile(
       "{\n\t"
-      ".reg .b32 p<32>;\n\t"
-      ".reg .b64 q<16>, sa, sb;\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {p0, p1, p2, p3, p4, p5, p6, p7, p8, p9, p10, p11, p12, p13, p14, p15}, [%8];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {p16, p17, p18, p19, p20, p21, p22, p23, p24, p25, p26, p27, p28, p29, p30, p31}, [%9];\n\t"
+      ".reg .f32 p<64>;\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {p0, p1, p2, p3, p4, p5, p6, p7, p8, p9, p10, p11, p12, p13, p14, p15, p16, p17, p18, p19, p20, p21, p22, p23, p24, p25, p26, p27, p28, p29, p30, p31}, [%32];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {p32, p33, p34, p35, p36, p37, p38, p39, p40, p41, p42, p43, p44, p45, p46, p47, p48, p49, p50, p51, p52, p53, p54, p55, p56, p57, p58, p59, p60, p61, p62, p63}, [%33];\n\t"
       "tcgen05.wait::ld.sync.aligned;\n\t"
-      "mov.b64 sa, {%10, %10};\n\t"
-      "mov.b64 sb, {%11, %11};\n\t"
-      "mov.b64 q0, {p0, p1};\n\tfma.rn.f32x2 %0, sa, q0, %0;\n\t"
-      "mov.b64 q1, {p2, p3};\n\tfma.rn.f32x2 %1, sa, q1, %1;\n\t"
-      "mov.b64 q2, {p4, p5};\n\tfma.rn.f32x2 %2, sa, q2, %2;\n\t"
-      "mov.b64 q3, {p6, p7};\n\tfma.rn.f32x2 %3, sa, q3, %3;\n\t"
-      "mov.b64 q4, {p8, p9};\n\tfma.rn.f32x2 %4, sa, q4, %4;\n\t"
-      "mov.b64 q5, {p10, p11};\n\tfma.rn.f32x2 %5, sa, q5, %5;\n\t"
-      "mov.b64 q6, {p12, p13};\n\tfma.rn.f32x2 %6, sa, q6, %6;\n\t"
-      "mov.b64 q7, {p14, p15};\n\tfma.rn.f32x2 %7, sa, q7, %7;\n\t"
-      "mov.b64 q8, {p16, p17};\n\tfma.rn.f32x2 %0, sb, q8, %0;\n\t"
-      "mov.b64 q9, {p18, p19};\n\tfma.rn.f32x2 %1, sb, q9, %1;\n\t"
-      "mov.b64 q10, {p20, p21};\n\tfma.rn.f32x2 %2, sb, q10, %2;\n\t"
-      "mov.b64 q11, {p22, p23};\n\tfma.rn.f32x2 %3, sb, q11, %3;\n\t"
-      "mov.b64 q12, {p24, p25};\n\tfma.rn.f32x2 %4, sb, q12, %4;\n\t"
-      "mov.b64 q13, {p26, p27};\n\tfma.rn.f32x2 %5, sb, q13, %5;\n\t"
-      "mov.b64 q14, {p28, p29};\n\tfma.rn.f32x2 %6, sb, q14, %6;\n\t"
-      "mov.b64 q15, {p30, p31};\n\tfma.rn.f32x2 %7, sb, q15, %7;\n\t"
+      "fma.rn.f32 %0, %34, p0, %0;\n\t"
+      "fma.rn.f32 %1, %34, p1, %1;\n\t"
+      "fma.rn.f32 %2, %34, p2, %2;\n\t"
+      "fma.rn.f32 %3, %34, p3, %3;\n\t"
+      "fma.rn.f32 %4, %34, p4, %4;\n\t"
+      "fma.rn.f32 %5, %34, p5, %5;\n\t"
+      "fma.rn.f32 %6, %34, p6, %6;\n\t"
+      "fma.rn.f32 %7, %34, p7, %7;\n\t"
+      "fma.rn.f32 %8, %34, p8, %8;\n\t"
+      "fma.rn.f32 %9, %34, p9, %9;\n\t"
+      "fma.rn.f32 %10, %34, p10, %10;\n\t"
+      "fma.rn.f32 %11, %34, p11, %11;\n\t"
+      "fma.rn.f32 %12, %34, p12, %12;\n\t"
+      "fma.rn.f32 %13, %34, p13, %13;\n\t"
+      "fma.rn.f32 %14, %34, p14, %14;\n\t"
+      "fma.rn.f32 %15, %34, p15, %15;\n\t"
+      "fma.rn.f32 %16, %34, p16, %16;\n\t"
+      "fma.rn.f32 %17, %34, p17, %17;\n\t"
+      "fma.rn.f32 %18, %34, p18, %18;\n\t"
+      "fma.rn.f32 %19, %34, p19, %19;\n\t"
+      "fma.rn.f32 %20, %34, p20, %20;\n\t"
+      "fma.rn.f32 %21, %34, p21, %21;\n\t"
+      "fma.rn.f32 %22, %34, p22, %22;\n\t"
+      "fma.rn.f32 %23, %34, p23, %23;\n\t"
+      "fma.rn.f32 %24, %34, p24, %24;\n\t"
+      "fma.rn.f32 %25, %34, p25, %25;\n\t"
+      "fma.rn.f32 %26, %34, p26, %26;\n\t"
+      "fma.rn.f32 %27, %34, p27, %27;\n\t"
+      "fma.rn.f32 %28, %34, p28, %28;\n\t"
+      "fma.rn.f32 %29, %34, p29, %29;\n\t"
+      "fma.rn.f32 %30, %34, p30, %30;\n\t"
+      "fma.rn.f32 %31, %34, p31, %31;\n\t"
+      "fma.rn.f32 %0, %35, p32, %0;\n\t"
+      "fma.rn.f32 %1, %35, p33, %1;\n\t"
+      "fma.rn.f32 %2, %35, p34, %2;\n\t"
+      "fma.rn.f32 %3, %35, p35, %3;\n\t"
+      "fma.rn.f32 %4, %35, p36, %4;\n\t"
+      "fma.rn.f32 %5, %35, p37, %5;\n\t"
+      "fma.rn.f32 %6, %35, p38, %6;\n\t"
+      "fma.rn.f32 %7, %35, p39, %7;\n\t"
+      "fma.rn.f32 %8, %35, p40, %8;\n\t"
+      "fma.rn.f32 %9, %35, p41, %9;\n\t"
+      "fma.rn.f32 %10, %35, p42, %10;\n\t"
+      "fma.rn.f32 %11, %35, p43, %11;\n\t"
+      "fma.rn.f32 %12, %35, p44, %12;\n\t"
+      "fma.rn.f32 %13, %35, p45, %13;\n\t"
+      "fma.rn.f32 %14, %35, p46, %14;\n\t"
+      "fma.rn.f32 %15, %35, p47, %15;\n\t"
+      "fma.rn.f32 %16, %35, p48, %16;\n\t"
+      "fma.rn.f32 %17, %35, p49, %17;\n\t"
+      "fma.rn.f32 %18, %35, p50, %18;\n\t"
+      "fma.rn.f32 %19, %35, p51, %19;\n\t"
+      "fma.rn.f32 %20, %35, p52, %20;\n\t"
+      "fma.rn.f32 %21, %35, p53, %21;\n\t"
+      "fma.rn.f32 %22, %35, p54, %22;\n\t"
+      "fma.rn.f32 %23, %35, p55, %23;\n\t"
+      "fma.rn.f32 %24, %35, p56, %24;\n\t"
+      "fma.rn.f32 %25, %35, p57, %25;\n\t"
+      "fma.rn.f32 %26, %35, p58, %26;\n\t"
+      "fma.rn.f32 %27, %35, p59, %27;\n\t"
+      "fma.rn.f32 %28, %35, p60, %28;\n\t"
+      "fma.rn.f32 %29, %35, p61, %29;\n\t"
+      "fma.rn.f32 %30, %35, p62, %30;\n\t"
+      "fma.rn.f32 %31, %35, p63, %31;\n\t"
       "}"
-      : "+l"(acc[0]), "+l"(acc[1]), "+l"(acc[2]), "+l"(acc[3]), "+l"(acc[4]),
-        "+l"(acc[5]), "+l"(acc[6]), "+l"(acc[7])
+      : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3]),
+        "+f"(acc[4]), "+f"(acc[5]), "+f"(acc[6]), "+f"(acc[7]),
+        "+f"(acc[8]), "+f"(acc[9]), "+f"(acc[10]), "+f"(acc[11]),
+        "+f"(acc[12]), "+f"(acc[13]), "+f"(acc[14]), "+f"(acc[15]),
+        "+f"(acc[16]), "+f"(acc[17]), "+f"(acc[18]), "+f"(acc[19]),
+        "+f"(acc[20]), "+f"(acc[21]), "+f"(acc[22]), "+f"(acc[23]),
+        "+f"(acc[24]), "+f"(acc[25]), "+f"(acc[26]), "+f"(acc[27]),
+        "+f"(acc[28]), "+f"(acc[29]), "+f"(acc[30]), "+f"(acc[31])
       : "r"(taddr0), "r"(taddr1), "f"(s0), "f"(s1)
       : "memory");
 }
@@ -290,18 +340,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ----------------------------------------------------------- promotion
     const int q = warp & 3;          // TMEM lane quarter = 32-row tile
-    const int cs = warp >> 2;        // 16-column slice of the 64-column tile
-    const int c = cs >> 1;           // its 32-column scale tile
+    const int c = warp >> 2;         // 32-column slice = column scale tile
     const uint32_t col0 = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                          16 * cs;
+                          32 * c;
     uint32_t s = 0, ph = 0, set = 0, sph = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
       int mb, nb;
       tile_coords(t, tiles_m, tiles_n, mb, nb);
-      uint64_t acc[8];    // packed FP32 pairs: columns 2j, 2j+1 of the slice
+      float acc[32];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] = 0;
+      for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
       for (int ks = 0; ok && ks < nks; ++ks) {
         // Scale products of this stage (acquired through the stage's full
         // barrier), then let the stage go as far as this warp is concerned.
@@ -328,34 +377,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t pbase = col0 + set * KPS * BN;
         // K blocks 0 and 1, then 2 and 3; after the second pair the whole
         // set is in registers and goes back to the MMA warp.
-        promote_pair16(acc, pbase, pbase + BN, sc.x, sc.y);
-        promote_pair16(acc, pbase + 2 * BN, pbase + 3 * BN, sc.z, sc.w);
+        promote_pair(acc, pbase, pbase + BN, sc.x, sc.y);
+        promote_pair(acc, pbase + 2 * BN, pbase + 3 * BN, sc.z, sc.w);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(pempty_bar(set));
         if (++set == NSETS) { set = 0; sph ^= 1u; }
       }
       if (!ok) break;
-      // Epilogue: round to BF16 and store this thread's 16 columns.
+      // Epilogue: round to BF16 and store this thread's 32 columns.
       const int row = mb * BM + q * 32 + lane;
-      const int n = nb * BN + 16 * cs;
+      const int n = nb * BN + 32 * c;
       if (row < a.M && n < a.N) {
         uint16_t *crow = a.C + static_cast<int64_t>(row) * a.ldc;
-        uint32_t w[8];
+        uint32_t w[16];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(
-              __uint_as_float(static_cast<uint32_t>(acc[j])),
-              __uint_as_float(static_cast<uint32_t>(acc[j] >> 32)));
+        for (int j = 0; j < 16; ++j) {
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
           w[j] = *reinterpret_cast<const uint32_t *>(&b2);
         }
-        if (a.c_vec16 && n + 16 <= a.N) {
+        if (a.c_vec16 && n + 32 <= a.N) {
           uint4 *dst = reinterpret_cast<uint4 *>(crow + n);
-          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2],
+                                w[4 * j + 3]);
         } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
+          for (int j = 0; j < 32; ++j)
             if (n + j < a.N)
               crow[n + j] = static_cast<uint16_t>(
                   (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu));

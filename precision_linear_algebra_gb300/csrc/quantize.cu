@@ -25,6 +25,10 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kBlocksPerSm = 4;
+// Bytes of x's tail that the amax pass asks L2 to keep for the cast pass
+// (L2 is 129 MB; the rest of it holds the codes being written and other
+// work's data).
+constexpr int64_t kL2KeepBytes = int64_t(64) << 20;
 
 // FP8 formats: 0 = E4M3 (max 448), 1 = E5M2 (max 57344).
 template <int FMT>
@@ -110,14 +114,40 @@ __device__ __forceinline__ float4 ld_stream4(const float4 *p) {
   return v;
 }
 
+// L2 eviction-priority policies for 128-bit loads.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ float4 ld_hint4(const float4 *p, uint64_t policy) {
+  float4 v;
+  asm volatile(
+      "ld.global.nc.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+      : "l"(p), "l"(policy));
+  return v;
+}
+
 // ------------------------------------------------------------------- amax
 // VEC = 4: x, ldx and cols allow 16-byte loads; VEC = 1: scalar loads.
 // A unit is VEC consecutive elements of one row; units are numbered row by
 // row, `upr` units per row.
+// `keep_from`: units at or past this index are loaded with an evict-last
+// L2 policy (the rest evict-first), so that the part of x the cast pass
+// reads first -- it walks the tensor backwards -- is still in L2.
 template <int VEC>
 __global__ void __launch_bounds__(kThreads)
     amax_kernel(const float *__restrict__ x, int64_t rows, int64_t upr,
-                int64_t ldx, bool contiguous, float *amax_out) {
+                int64_t ldx, bool contiguous, int64_t keep_from,
+                float *amax_out) {
   const int64_t n = rows * upr;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -125,15 +155,18 @@ __global__ void __launch_bounds__(kThreads)
   if (VEC == 4) {
     if (contiguous) {
       const float4 *x4 = reinterpret_cast<const float4 *>(x);
+      const uint64_t keep = policy_evict_last(), drop = policy_evict_first();
       for (; i + 3 * stride < n; i += 4 * stride) {
-        const float4 a = ld_stream4(x4 + i);
-        const float4 b = ld_stream4(x4 + i + stride);
-        const float4 c = ld_stream4(x4 + i + 2 * stride);
-        const float4 d = ld_stream4(x4 + i + 3 * stride);
+        const uint64_t pol = i + 3 * stride >= keep_from ? keep : drop;
+        const float4 a = ld_hint4(x4 + i, pol);
+        const float4 b = ld_hint4(x4 + i + stride, pol);
+        const float4 c = ld_hint4(x4 + i + 2 * stride, pol);
+        const float4 d = ld_hint4(x4 + i + 3 * stride, pol);
         m = max_abs4(max_abs4(m, a), b);
         m = max_abs4(max_abs4(m, c), d);
       }
-      for (; i < n; i += stride) m = max_abs4(m, ld_stream4(x4 + i));
+      for (; i < n; i += stride)
+        m = max_abs4(m, ld_hint4(x4 + i, i >= keep_from ? keep : drop));
     } else {
       for (; i < n; i += stride) {
         const int64_t r = i / upr, c = i - r * upr;
@@ -169,17 +202,19 @@ __global__ void __launch_bounds__(kThreads)
       const float4 *x4 = reinterpret_cast<const float4 *>(x);
       uint32_t *q4 = reinterpret_cast<uint32_t *>(q);
       const int64_t last = n - 1;
+      const uint64_t drop = policy_evict_first();   // last use of x
       for (; i + 3 * stride < n; i += 4 * stride) {
-        const float4 a = ld_stream4(x4 + (last - i));
-        const float4 b = ld_stream4(x4 + (last - i - stride));
-        const float4 c = ld_stream4(x4 + (last - i - 2 * stride));
-        const float4 d = ld_stream4(x4 + (last - i - 3 * stride));
+        const float4 a = ld_hint4(x4 + (last - i), drop);
+        const float4 b = ld_hint4(x4 + (last - i - stride), drop);
+        const float4 c = ld_hint4(x4 + (last - i - 2 * stride), drop);
+        const float4 d = ld_hint4(x4 + (last - i - 3 * stride), drop);
         q4[last - i] = cvt4<FMT>(a, qs);
         q4[last - i - stride] = cvt4<FMT>(b, qs);
         q4[last - i - 2 * stride] = cvt4<FMT>(c, qs);
         q4[last - i - 3 * stride] = cvt4<FMT>(d, qs);
       }
-      for (; i < n; i += stride) q4[last - i] = cvt4<FMT>(ld_stream4(x4 + (last - i)), qs);
+      for (; i < n; i += stride)
+        q4[last - i] = cvt4<FMT>(ld_hint4(x4 + (last - i), drop), qs);
     } else {
       for (; i < n; i += stride) {
         const int64_t r = i / upr, c = i - r * upr;
@@ -308,13 +343,17 @@ fp8la_status quantize_pertensor_impl(const float *x, int64_t rows,
   if (vec4) {
     const int64_t upr = cols / 4;
     const int g = grid_for(rows * upr, kThreads);
+    // Keep up to kL2KeepBytes of x's tail resident for the cast pass.
+    const int64_t units = rows * upr;
+    const int64_t keep_units = kL2KeepBytes / 16;
+    const int64_t keep_from = units > keep_units ? units - keep_units : 0;
     amax_kernel<4><<<g, kThreads, 0, s>>>(x, rows, upr, ldx, contiguous,
-                                          amax_out);
+                                          keep_from, amax_out);
     cast_kernel<4, FMT><<<g, kThreads, 0, s>>>(x, rows, upr, ldx, q, ldq,
                                                contiguous, amax_out, scale_out);
   } else {
     const int g = grid_for(rows * cols, kThreads);
-    amax_kernel<1><<<g, kThreads, 0, s>>>(x, rows, cols, ldx, contiguous,
+    amax_kernel<1><<<g, kThreads, 0, s>>>(x, rows, cols, ldx, contiguous, 0,
                                           amax_out);
     cast_kernel<1, FMT><<<g, kThreads, 0, s>>>(x, rows, cols, ldx, q, ldq,
                                                contiguous, amax_out, scale_out);
