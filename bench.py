@@ -549,8 +549,71 @@ def _workload_grouped(fl, torch, dev, sptr, ph):
                 qprofile=("quantize_pertensor_8192", QUANT_SOURCES))
 
 
+def _workload_attention(fl, torch, dev, sptr, ph, batch=2, heads=64, seq=2048, hd=128):
+    """The two GEMMs of non-causal FP8 multi-head attention, one group per
+    (batch, head): scores = Q K^T (K = head_dim) and out = P V (K = seq, V
+    given transposed).  Q, K, P and V are quantised to E4M3 per head once,
+    at set-up (the quantiser is measured by the other workloads); a step is
+    the two grouped GEMM launches.  Softmax is not part of this path: P is a
+    seeded stand-in for the probabilities."""
+    import numpy as np
+    from precision_linear_algebra_gb300 import workloads
+    E = batch * heads
+    g = np.random.default_rng(0)
+    Q_np = workloads.normal(g, (E * seq, hd))
+    K_np = workloads.normal(g, (E, seq, hd))
+    P_np = g.random((E * seq, seq), dtype=np.float32) / np.float32(seq)
+    Vt_np = workloads.normal(g, (E, hd, seq))
+    qQ = torch.empty(Q_np.shape, dtype=torch.uint8, device=dev)
+    qK = torch.empty(K_np.shape, dtype=torch.uint8, device=dev)
+    qP = torch.empty(P_np.shape, dtype=torch.uint8, device=dev)
+    qV = torch.empty(Vt_np.shape, dtype=torch.uint8, device=dev)
+    amax = torch.empty(4 * E, dtype=torch.float32, device=dev)
+    sc = torch.empty(4 * E, dtype=torch.float32, device=dev)
+    Pp = lambda t, i=0: t.data_ptr() + i * t.element_size()
+    for arr, q, k4, rows, cols in ((Q_np, qQ, 0, seq, hd), (K_np, qK, 1, seq, hd),
+                                   (P_np, qP, 2, seq, seq), (Vt_np, qV, 3, hd, seq)):
+        x = torch.from_numpy(arr).to(dev)
+        for e in range(E):
+            fl.fp8_quantize_pertensor(Pp(x, e * rows * cols), rows, cols, cols,
+                                      Pp(q, e * rows * cols), cols, Pp(amax, k4 * E + e),
+                                      Pp(sc, k4 * E + e), sptr)
+        torch.cuda.synchronize()
+        del x
+    offs = torch.arange(E + 1, dtype=torch.int32, device=dev) * seq
+    S = torch.empty((E * seq, seq), dtype=torch.bfloat16, device=dev)
+    O = torch.empty((E * seq, hd), dtype=torch.bfloat16, device=dev)
+
+    def step():
+        ph.mark("quant")
+        ph.mark("quant")
+        ph.mark("gemm")
+        fl.fp8_grouped_gemm(E, offs.data_ptr(), E * seq, Pp(qQ), hd, Pp(qK), hd, seq * hd,
+                            Pp(S), seq, seq, hd, Pp(sc, 0), Pp(sc, E), sptr)
+        fl.fp8_grouped_gemm(E, offs.data_ptr(), E * seq, Pp(qP), seq, Pp(qV), seq, hd * seq,
+                            Pp(O), hd, hd, seq, Pp(sc, 2 * E), Pp(sc, 3 * E), sptr)
+        ph.mark("gemm")
+
+    flops = 2.0 * 2 * E * seq * seq * hd
+    codes = [(qQ, qQ.cpu().numpy()), (qK, qK.cpu().numpy()), (qP, qP.cpu().numpy()),
+             (qV, qV.cpu().numpy())]
+    return dict(step=step, flops=flops, launches=2,
+                workload=("FP8 attention GEMMs (scores = Q K^T, out = P V), non-causal, batch %d x "
+                          "%d heads, seq %d, head_dim %d, E4M3 inputs with per-head scales "
+                          "(quantised at set-up); two grouped launches per step; seed 0"
+                          % (batch, heads, seq, hd)),
+                config={"batch": batch, "heads": heads, "seq": seq, "head_dim": hd,
+                        "l2": "operands 0.64 GB + outputs 1.14 GB > 129 MB L2; no flush"},
+                inputs=codes, outputs=[S, O], quant_elems=1,
+                gemm_label="gemm_e4m3_pair_kernel<true>",
+                gemm_bytes=qQ.numel() + qK.numel() + qP.numel() + qV.numel() + 2 * (S.numel() + O.numel()),
+                profile=("gemm_e4m3_attention", GEMM_SOURCES),
+                qprofile=("quantize_pertensor_8192", QUANT_SOURCES))
+
+
 WORKLOADS = {"pertensor8192": _workload_pertensor, "blockscaled": _workload_blockscaled,
-             "grouped": _workload_grouped, "square256": _workload_square(256),
+             "grouped": _workload_grouped, "attention": _workload_attention,
+             "square256": _workload_square(256),
              "square1024": _workload_square(1024)}
 
 
@@ -711,9 +774,12 @@ def run_gpu(args):
     g_avg = statistics.mean(g_ms)
     q_avg = statistics.mean(q_ms)
     gemm_tflops = W["flops"] / (g_avg * 1e-3) / 1e12
-    quant_gbs = QUANT_BYTES_PER_ELEM * W["quant_elems"] / (q_avg * 1e-3) / 1e9
+    quant_gbs = (QUANT_BYTES_PER_ELEM * W["quant_elems"] / (q_avg * 1e-3) / 1e9
+                 if q_avg > 1e-6 else None)
     if args.workload == "blockscaled":
         quant_gbs = 5 * W["quant_elems"] / (q_avg * 1e-3) / 1e9   # one pass: 4 B read + 1 B written
+    if args.workload == "attention":
+        quant_gbs = None                                           # quantised at set-up
 
     if rank == 0:
         line = {
@@ -733,7 +799,8 @@ def run_gpu(args):
                          "frac_of_sustained": (gemm_tflops / (bf16_sust * FP8_OVER_BF16)
                                                if bf16_sust else None)},
             "roofline_quantize": {"bound": "hbm", "achieved": quant_gbs, "peak": hbm,
-                                  "unit": "GB/s", "frac": quant_gbs / hbm,
+                                  "unit": "GB/s",
+                                  "frac": quant_gbs / hbm if quant_gbs else None,
                                   "traffic": _profile_traffic(*W["qprofile"]),
                                   "algorithmic_bytes_per_elem":
                                       5 if args.workload == "blockscaled" else QUANT_BYTES_PER_ELEM},
