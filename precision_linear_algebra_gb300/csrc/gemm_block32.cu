@@ -32,10 +32,9 @@
 //     columns 32(w/4)..+31 of each partial, exactly one 32 x 32 scale tile,
 //     so its scale is one number per K block: sa * sb from two 16-byte
 //     shared-memory vectors per stage.  Each thread keeps its row's 32 FP32 accumulators in
-//     registers and adds (sa*sb) * partial with scalar FP32 FMAs, two K
-//     blocks' partials per TMEM wait, each pair of K blocks in one asm
-//     statement (packed f32x2 FMAs would need the loaded registers moved
-//     into pairs first, costing more issue slots than they save).  After the last stage of a tile it
+//     registers (as 16 packed pairs) and adds (sa*sb) * partial with packed
+//     FMAs (fma.rn.f32x2), two K blocks' partials per TMEM wait, each pair
+//     of K blocks in one asm statement.  After the last stage of a tile it
 //     rounds to BF16 and stores 64 bytes.
 //   * A stage is recycled only when its MMAs have completed and all eight
 //     promotion warps have read its scales (empty count 1 + 8); a
@@ -120,92 +119,60 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n,
   nb = r / gm;
 }
 
-// Promotion of two K blocks' partials, 32 columns of one lane row each:
+// Promotion of two K blocks' partials (32 columns each, one lane row):
 // loads both from TMEM, waits, and adds s0 * first + s1 * second into the
-// thread's 32 FP32 accumulators with scalar FMAs (fma.rn.f32, one rounding
-// each).  One asm statement, so the loaded values never leave it.
-__device__ __forceinline__ void promote_pair(float (&acc)[32], uint32_t taddr0,
-                                             uint32_t taddr1, float s0,
-                                             float s1) {
+// 32 FP32 accumulators held as 16 packed pairs (acc[j] = columns 2j, 2j+1),
+// with packed FMAs fma.rn.f32x2 (each lane of a pair rounded once).  One
+// asm statement, so the loaded values never leave it.
+__device__ __forceinline__ void promote_pair(uint64_t (&acc)[16],
+                                             uint32_t taddr0, uint32_t taddr1,
+                                             float s0, float s1) {
   asm volatile(
       "{\n\t"
-      ".reg .f32 p<64>;\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {p0, p1, p2, p3, p4, p5, p6, p7, p8, p9, p10, p11, p12, p13, p14, p15, p16, p17, p18, p19, p20, p21, p22, p23, p24, p25, p26, p27, p28, p29, p30, p31}, [%32];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {p32, p33, p34, p35, p36, p37, p38, p39, p40, p41, p42, p43, p44, p45, p46, p47, p48, p49, p50, p51, p52, p53, p54, p55, p56, p57, p58, p59, p60, p61, p62, p63}, [%33];\n\t"
+      ".reg .b32 p<64>;\n\t"
+      ".reg .b64 q<32>, sa, sb;\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {p0, p1, p2, p3, p4, p5, p6, p7, p8, p9, p10, p11, p12, p13, p14, p15, p16, p17, p18, p19, p20, p21, p22, p23, p24, p25, p26, p27, p28, p29, p30, p31}, [%16];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {p32, p33, p34, p35, p36, p37, p38, p39, p40, p41, p42, p43, p44, p45, p46, p47, p48, p49, p50, p51, p52, p53, p54, p55, p56, p57, p58, p59, p60, p61, p62, p63}, [%17];\n\t"
       "tcgen05.wait::ld.sync.aligned;\n\t"
-      "fma.rn.f32 %0, %34, p0, %0;\n\t"
-      "fma.rn.f32 %1, %34, p1, %1;\n\t"
-      "fma.rn.f32 %2, %34, p2, %2;\n\t"
-      "fma.rn.f32 %3, %34, p3, %3;\n\t"
-      "fma.rn.f32 %4, %34, p4, %4;\n\t"
-      "fma.rn.f32 %5, %34, p5, %5;\n\t"
-      "fma.rn.f32 %6, %34, p6, %6;\n\t"
-      "fma.rn.f32 %7, %34, p7, %7;\n\t"
-      "fma.rn.f32 %8, %34, p8, %8;\n\t"
-      "fma.rn.f32 %9, %34, p9, %9;\n\t"
-      "fma.rn.f32 %10, %34, p10, %10;\n\t"
-      "fma.rn.f32 %11, %34, p11, %11;\n\t"
-      "fma.rn.f32 %12, %34, p12, %12;\n\t"
-      "fma.rn.f32 %13, %34, p13, %13;\n\t"
-      "fma.rn.f32 %14, %34, p14, %14;\n\t"
-      "fma.rn.f32 %15, %34, p15, %15;\n\t"
-      "fma.rn.f32 %16, %34, p16, %16;\n\t"
-      "fma.rn.f32 %17, %34, p17, %17;\n\t"
-      "fma.rn.f32 %18, %34, p18, %18;\n\t"
-      "fma.rn.f32 %19, %34, p19, %19;\n\t"
-      "fma.rn.f32 %20, %34, p20, %20;\n\t"
-      "fma.rn.f32 %21, %34, p21, %21;\n\t"
-      "fma.rn.f32 %22, %34, p22, %22;\n\t"
-      "fma.rn.f32 %23, %34, p23, %23;\n\t"
-      "fma.rn.f32 %24, %34, p24, %24;\n\t"
-      "fma.rn.f32 %25, %34, p25, %25;\n\t"
-      "fma.rn.f32 %26, %34, p26, %26;\n\t"
-      "fma.rn.f32 %27, %34, p27, %27;\n\t"
-      "fma.rn.f32 %28, %34, p28, %28;\n\t"
-      "fma.rn.f32 %29, %34, p29, %29;\n\t"
-      "fma.rn.f32 %30, %34, p30, %30;\n\t"
-      "fma.rn.f32 %31, %34, p31, %31;\n\t"
-      "fma.rn.f32 %0, %35, p32, %0;\n\t"
-      "fma.rn.f32 %1, %35, p33, %1;\n\t"
-      "fma.rn.f32 %2, %35, p34, %2;\n\t"
-      "fma.rn.f32 %3, %35, p35, %3;\n\t"
-      "fma.rn.f32 %4, %35, p36, %4;\n\t"
-      "fma.rn.f32 %5, %35, p37, %5;\n\t"
-      "fma.rn.f32 %6, %35, p38, %6;\n\t"
-      "fma.rn.f32 %7, %35, p39, %7;\n\t"
-      "fma.rn.f32 %8, %35, p40, %8;\n\t"
-      "fma.rn.f32 %9, %35, p41, %9;\n\t"
-      "fma.rn.f32 %10, %35, p42, %10;\n\t"
-      "fma.rn.f32 %11, %35, p43, %11;\n\t"
-      "fma.rn.f32 %12, %35, p44, %12;\n\t"
-      "fma.rn.f32 %13, %35, p45, %13;\n\t"
-      "fma.rn.f32 %14, %35, p46, %14;\n\t"
-      "fma.rn.f32 %15, %35, p47, %15;\n\t"
-      "fma.rn.f32 %16, %35, p48, %16;\n\t"
-      "fma.rn.f32 %17, %35, p49, %17;\n\t"
-      "fma.rn.f32 %18, %35, p50, %18;\n\t"
-      "fma.rn.f32 %19, %35, p51, %19;\n\t"
-      "fma.rn.f32 %20, %35, p52, %20;\n\t"
-      "fma.rn.f32 %21, %35, p53, %21;\n\t"
-      "fma.rn.f32 %22, %35, p54, %22;\n\t"
-      "fma.rn.f32 %23, %35, p55, %23;\n\t"
-      "fma.rn.f32 %24, %35, p56, %24;\n\t"
-      "fma.rn.f32 %25, %35, p57, %25;\n\t"
-      "fma.rn.f32 %26, %35, p58, %26;\n\t"
-      "fma.rn.f32 %27, %35, p59, %27;\n\t"
-      "fma.rn.f32 %28, %35, p60, %28;\n\t"
-      "fma.rn.f32 %29, %35, p61, %29;\n\t"
-      "fma.rn.f32 %30, %35, p62, %30;\n\t"
-      "fma.rn.f32 %31, %35, p63, %31;\n\t"
+      "mov.b64 sa, {%18, %18};\n\t"
+      "mov.b64 sb, {%19, %19};\n\t"
+      "mov.b64 q0, {p0, p1};\n\tfma.rn.f32x2 %0, sa, q0, %0;\n\t"
+      "mov.b64 q1, {p2, p3};\n\tfma.rn.f32x2 %1, sa, q1, %1;\n\t"
+      "mov.b64 q2, {p4, p5};\n\tfma.rn.f32x2 %2, sa, q2, %2;\n\t"
+      "mov.b64 q3, {p6, p7};\n\tfma.rn.f32x2 %3, sa, q3, %3;\n\t"
+      "mov.b64 q4, {p8, p9};\n\tfma.rn.f32x2 %4, sa, q4, %4;\n\t"
+      "mov.b64 q5, {p10, p11};\n\tfma.rn.f32x2 %5, sa, q5, %5;\n\t"
+      "mov.b64 q6, {p12, p13};\n\tfma.rn.f32x2 %6, sa, q6, %6;\n\t"
+      "mov.b64 q7, {p14, p15};\n\tfma.rn.f32x2 %7, sa, q7, %7;\n\t"
+      "mov.b64 q8, {p16, p17};\n\tfma.rn.f32x2 %8, sa, q8, %8;\n\t"
+      "mov.b64 q9, {p18, p19};\n\tfma.rn.f32x2 %9, sa, q9, %9;\n\t"
+      "mov.b64 q10, {p20, p21};\n\tfma.rn.f32x2 %10, sa, q10, %10;\n\t"
+      "mov.b64 q11, {p22, p23};\n\tfma.rn.f32x2 %11, sa, q11, %11;\n\t"
+      "mov.b64 q12, {p24, p25};\n\tfma.rn.f32x2 %12, sa, q12, %12;\n\t"
+      "mov.b64 q13, {p26, p27};\n\tfma.rn.f32x2 %13, sa, q13, %13;\n\t"
+      "mov.b64 q14, {p28, p29};\n\tfma.rn.f32x2 %14, sa, q14, %14;\n\t"
+      "mov.b64 q15, {p30, p31};\n\tfma.rn.f32x2 %15, sa, q15, %15;\n\t"
+      "mov.b64 q16, {p32, p33};\n\tfma.rn.f32x2 %0, sb, q16, %0;\n\t"
+      "mov.b64 q17, {p34, p35};\n\tfma.rn.f32x2 %1, sb, q17, %1;\n\t"
+      "mov.b64 q18, {p36, p37};\n\tfma.rn.f32x2 %2, sb, q18, %2;\n\t"
+      "mov.b64 q19, {p38, p39};\n\tfma.rn.f32x2 %3, sb, q19, %3;\n\t"
+      "mov.b64 q20, {p40, p41};\n\tfma.rn.f32x2 %4, sb, q20, %4;\n\t"
+      "mov.b64 q21, {p42, p43};\n\tfma.rn.f32x2 %5, sb, q21, %5;\n\t"
+      "mov.b64 q22, {p44, p45};\n\tfma.rn.f32x2 %6, sb, q22, %6;\n\t"
+      "mov.b64 q23, {p46, p47};\n\tfma.rn.f32x2 %7, sb, q23, %7;\n\t"
+      "mov.b64 q24, {p48, p49};\n\tfma.rn.f32x2 %8, sb, q24, %8;\n\t"
+      "mov.b64 q25, {p50, p51};\n\tfma.rn.f32x2 %9, sb, q25, %9;\n\t"
+      "mov.b64 q26, {p52, p53};\n\tfma.rn.f32x2 %10, sb, q26, %10;\n\t"
+      "mov.b64 q27, {p54, p55};\n\tfma.rn.f32x2 %11, sb, q27, %11;\n\t"
+      "mov.b64 q28, {p56, p57};\n\tfma.rn.f32x2 %12, sb, q28, %12;\n\t"
+      "mov.b64 q29, {p58, p59};\n\tfma.rn.f32x2 %13, sb, q29, %13;\n\t"
+      "mov.b64 q30, {p60, p61};\n\tfma.rn.f32x2 %14, sb, q30, %14;\n\t"
+      "mov.b64 q31, {p62, p63};\n\tfma.rn.f32x2 %15, sb, q31, %15;\n\t"
       "}"
-      : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3]),
-        "+f"(acc[4]), "+f"(acc[5]), "+f"(acc[6]), "+f"(acc[7]),
-        "+f"(acc[8]), "+f"(acc[9]), "+f"(acc[10]), "+f"(acc[11]),
-        "+f"(acc[12]), "+f"(acc[13]), "+f"(acc[14]), "+f"(acc[15]),
-        "+f"(acc[16]), "+f"(acc[17]), "+f"(acc[18]), "+f"(acc[19]),
-        "+f"(acc[20]), "+f"(acc[21]), "+f"(acc[22]), "+f"(acc[23]),
-        "+f"(acc[24]), "+f"(acc[25]), "+f"(acc[26]), "+f"(acc[27]),
-        "+f"(acc[28]), "+f"(acc[29]), "+f"(acc[30]), "+f"(acc[31])
+      : "+l"(acc[0]), "+l"(acc[1]), "+l"(acc[2]), "+l"(acc[3]), "+l"(acc[4]),
+        "+l"(acc[5]), "+l"(acc[6]), "+l"(acc[7]), "+l"(acc[8]), "+l"(acc[9]),
+        "+l"(acc[10]), "+l"(acc[11]), "+l"(acc[12]), "+l"(acc[13]),
+        "+l"(acc[14]), "+l"(acc[15])
       : "r"(taddr0), "r"(taddr1), "f"(s0), "f"(s1)
       : "memory");
 }
@@ -340,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ----------------------------------------------------------- promotion
     const int q = warp & 3;          // TMEM lane quarter = 32-row tile
-    const int c = warp >> 2;         // 32-column slice = column scale tile
+    const int c = warp >> 2;         // 32-column slice = column tile
     const uint32_t col0 = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                           32 * c;
     uint32_t s = 0, ph = 0, set = 0, sph = 0;
@@ -348,9 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
       int mb, nb;
       tile_coords(t, tiles_m, tiles_n, mb, nb);
-      float acc[32];
+      uint64_t acc[16];   // packed FP32 pairs: columns 2j, 2j+1
 #pragma unroll
-      for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < 16; ++j) acc[j] = 0;
       for (int ks = 0; ok && ks < nks; ++ks) {
         // Scale products of this stage (acquired through the stage's full
         // barrier), then let the stage go as far as this warp is concerned.
@@ -393,7 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t w[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(
+              __uint_as_float(static_cast<uint32_t>(acc[j])),
+              __uint_as_float(static_cast<uint32_t>(acc[j] >> 32)));
           w[j] = *reinterpret_cast<const uint32_t *>(&b2);
         }
         if (a.c_vec16 && n + 32 <= a.N) {
