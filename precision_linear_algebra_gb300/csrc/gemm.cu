@@ -62,6 +62,7 @@ struct GemmArgs {
   int32_t withhold_first;  // diagnostic: skip the first TMA arrival
   int32_t c_vec16;         // C rows allow 16-byte stores (C 16-byte aligned, ldc % 8 == 0)
   uint32_t fmt_bits;       // operand-format bits of the MMA instruction descriptor
+  int32_t split_tail;      // CTA-pair kernel: last tiles computed as two 128-column halves
 };
 
 template <int BN, int STAGES>
@@ -380,13 +381,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 // issues M=256, N=256, K=32 MMAs that read both CTAs' shared memory and
 // accumulate into both CTAs' tensor memory (CTA r holds rows 128r.. of the
 // tile, all 256 columns).  Per SM this halves the B bytes moved per MMA
-// FLOP compared with the single-CTA 128 x 256 tile.  Both CTAs' TMA loads
+// FLOP compared with the single-CTA 128 x 256 tile.  When the last wave of
+// tiles would fill at most half the clusters, those tiles are computed as
+// two 256 x 128 halves (N = 128 MMAs, 64 B rows per CTA), so the tail takes
+// half a tile's time.  Both CTAs' TMA loads
 // complete on the leader's `full` barrier; the leader's commits are
 // multicast to both CTAs' `empty` / `tmem_full` barriers; both CTAs'
 // epilogue warps release an accumulator on the leader's `tmem_empty`.
 constexpr int P_BM = 256;   // tile rows per CTA pair
 constexpr int P_BN = 256;   // tile columns per CTA pair
 constexpr int P_STAGES = 6;
+// Warps 0-3 and 6-9 are epilogue warps (two per TMEM lane quarter, each
+// storing half of the tile's columns); warp 4 loads, warp 5 issues MMAs.
+constexpr int P_THREADS = 320;
+constexpr int P_EPI_WARPS = 8;
 
 struct PairSmem {
   static constexpr int kABytes = 128 * BK;   // this CTA's half of A
@@ -409,9 +417,10 @@ static_assert(PairSmem::kB % 1024 == 0 && PairSmem::kABytes % 1024 == 0 &&
 static_assert(PairSmem::kAlloc <= 227 * 1024, "shared memory");
 
 template <bool GROUPED>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(P_THREADS, 1)
     gemm_e4m3_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmB64,
                           const GemmArgs a) {
   using L = PairSmem;
   constexpr int STAGES = P_STAGES;
@@ -449,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), 8);  // 4 epilogue warps in each CTA
+      mbar_init(tempty_bar(b), 2 * P_EPI_WARPS);  // epilogue warps of both CTAs
     }
     mbar_init(final_bar, 1);
     *abort_flag = 0;
@@ -458,6 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 4 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (a.split_tail > 0) tma_prefetch_desc(&tmB64);
   }
   if (warp == 5) {
     tmem_alloc_pair(smem_addr(tmem_slot), L::kTmemCols);
@@ -483,17 +493,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int total_tiles = GROUPED ? pref[a.num_groups]
                                   : ((a.M + P_BM - 1) / P_BM) * tiles_n;
+  // Work items: the first total_tiles - split tiles whole, the last `split`
+  // tiles as two 256 x 128 halves each (so that a last, partly filled wave
+  // of tiles takes half as long).
+  const int split = GROUPED ? 0 : a.split_tail;
+  const int n_whole = total_tiles - split;
+  const int n_items = n_whole + 2 * split;
+  // Item i -> its tile and half (-1 = whole tile).
+  auto item = [&](int i, int &half) {
+    int t = i;
+    half = -1;
+    if (i >= n_whole) {
+      t = n_whole + ((i - n_whole) >> 1);
+      half = (i - n_whole) & 1;
+    }
+    TileInfo ti = tile_info<GROUPED, P_BM>(t, a, tiles_n, pref, offs_smem, P_BN);
+    if (half >= 0) ti.n0 += 128 * half;
+    return ti;
+  };
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t s = 0, ph = 0, issued = 0;
       bool ok = true;
-      for (int t = cluster_id; ok && t < total_tiles; t += num_clusters) {
-        const TileInfo ti =
-            tile_info<GROUPED, P_BM>(t, a, tiles_n, pref, offs_smem, P_BN);
+      for (int i = cluster_id; ok && i < n_items; i += num_clusters) {
+        int half;
+        const TileInfo ti = item(i, half);
+        // A whole tile takes 128 B rows per CTA, a half tile 64.
+        const int brows = half < 0 ? 128 : 64;
         const int arow = ti.row0 + 128 * static_cast<int>(rank);
-        const int brow = ti.n0 + 128 * static_cast<int>(rank);
+        const int brow = ti.n0 + brows * static_cast<int>(rank);
+        const uint32_t bytes = 2u * (L::kABytes + brows * BK);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns, a.status,
                          abort_flag)) {
@@ -501,15 +532,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t lf = mapa_shared(full_bar(s), 0);
-          if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * L::kStageBytes);
+          if (leader) mbar_arrive_expect_tx(full_bar(s), bytes);
           tma_load_2d_pair(base + L::kA + s * L::kABytes, &tmA, lf, kb * BK,
                            arow);
           if (GROUPED)
             tma_load_3d_pair(base + L::kB + s * L::kBBytes, &tmB, lf, kb * BK,
                              brow, ti.group);
           else
-            tma_load_2d_pair(base + L::kB + s * L::kBBytes, &tmB, lf, kb * BK,
-                             brow);
+            tma_load_2d_pair(base + L::kB + s * L::kBBytes,
+                             half < 0 ? &tmB : &tmB64, lf, kb * BK, brow);
           ++issued;
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
@@ -527,11 +558,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 5) {
     // ------------------------------------------------- MMA (leader CTA only)
     if (lane == 0 && leader) {
-      const uint32_t idesc = idesc_e4m3_f32(P_BM, P_BN) | a.fmt_bits;
+      const uint32_t idesc_whole = idesc_e4m3_f32(P_BM, P_BN) | a.fmt_bits;
+      const uint32_t idesc_half = idesc_e4m3_f32(P_BM, P_BN / 2) | a.fmt_bits;
       uint32_t s = 0, ph = 0, local = 0;
       bool ok = true;
-      for (int t = cluster_id; ok && t < total_tiles;
-           t += num_clusters, ++local) {
+      for (int i = cluster_id; ok && i < n_items; i += num_clusters, ++local) {
+        const uint32_t idesc = i < n_whole ? idesc_whole : idesc_half;
         const uint32_t buf = local & 1u, use = local >> 1;
         if (!mbar_wait(tempty_bar(buf), (use & 1u) ^ 1u, a.timeout_ns,
                        a.status, abort_flag)) {
@@ -571,9 +603,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     int cur_group = -1;
     const uint32_t leader_tempty0 = mapa_shared(tempty_bar(0), 0);
     const uint32_t leader_tempty1 = mapa_shared(tempty_bar(1), 0);
-    for (int t = cluster_id; t < total_tiles; t += num_clusters, ++local) {
-      const TileInfo ti =
-          tile_info<GROUPED, P_BM>(t, a, tiles_n, pref, offs_smem, P_BN);
+    const int quarter = warp & 3;                 // TMEM lanes 32*quarter..
+    const int col_half = warp >= 6 ? 1 : 0;       // which half of the columns
+    for (int i = cluster_id; i < n_items; i += num_clusters, ++local) {
+      int half;
+      const TileInfo ti = item(i, half);
+      const int width = (half < 0 ? P_BN : P_BN / 2) / 2;   // this warp's share
+      const int col0 = col_half * width;
       if (ti.group != cur_group) {
         scale = __fmul_rn(a.scale_a[ti.group], a.scale_b[ti.group]);
         cur_group = ti.group;
@@ -583,14 +619,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    a.status, abort_flag);
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after();
-      const int row = ti.row0 + 128 * static_cast<int>(rank) + warp * 32 + lane;
+      const int row =
+          ti.row0 + 128 * static_cast<int>(rank) + quarter * 32 + lane;
       const bool row_ok = row < ti.row_end;
       uint16_t *crow = a.C + static_cast<int64_t>(row) * a.ldc;
-      const uint32_t taddr =
-          tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + buf * P_BN;
+      const uint32_t taddr = tmem_base +
+                             (static_cast<uint32_t>(quarter * 32) << 16) +
+                             buf * P_BN + col0;
 #pragma unroll 1
-      for (int c = 0; c < P_BN; c += 32)
-        store_chunk32(taddr + c, row_ok, crow, ti.n0 + c, a.N, scale,
+      for (int c = 0; c < width; c += 32)
+        store_chunk32(taddr + c, row_ok, crow, ti.n0 + col0 + c, a.N, scale,
                       a.c_vec16 != 0);
       tc_fence_before();
       __syncwarp();
@@ -691,8 +729,8 @@ fp8la_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB,
 // can be resident at once (at most one per pair tile).
 template <bool GROUPED>
 fp8la_status launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB,
-                              const GemmArgs &args, int64_t max_tiles,
-                              cudaStream_t s) {
+                              const CUtensorMap &tmB64, GemmArgs args,
+                              int64_t max_tiles, cudaStream_t s) {
   using L = PairSmem;
   auto kern = gemm_e4m3_pair_kernel<GROUPED>;
   const int slot = GROUPED ? 3 : 2;
@@ -707,7 +745,7 @@ fp8la_status launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB,
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(P_THREADS, 1, 1);
   cfg.dynamicSmemBytes = L::kAlloc;
   cfg.stream = s;
   cfg.attrs = attr;
@@ -720,10 +758,18 @@ fp8la_status launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB,
       return FP8LA_ERR_CUDA;
     cache_clusters(slot, clusters);
   }
-  int64_t n = max_tiles < clusters ? max_tiles : clusters;
+  // Split the tiles of a last, at most half-filled wave into halves (for
+  // the per-tensor GEMM, where max_tiles is the exact tile count).
+  args.split_tail = 0;
+  if (!GROUPED) {
+    const int64_t rem = max_tiles % clusters;
+    if (rem > 0 && 2 * rem <= clusters) args.split_tail = static_cast<int32_t>(rem);
+  }
+  const int64_t items = max_tiles + args.split_tail;
+  int64_t n = items < clusters ? items : clusters;
   if (n < 1) n = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * n), 1, 1);
-  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, args) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmB64, args) != cudaSuccess)
     return FP8LA_ERR_CUDA;
   return launch_status();
 }
@@ -770,9 +816,10 @@ fp8la_status gemm_pertensor_impl(const uint8_t *A, int64_t lda,
   // path always uses the single-CTA kernel.
   const int v = g_variant.load();
   const bool pair = !withhold && (v == 2 || (v == 0 && M > BM));
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tmB64;
   if (!encode_2d(&tmA, A, K, M, lda, BK, BM) ||
-      !encode_2d(&tmB, B, K, N, ldb, BK, pair ? 128 : kBN))
+      !encode_2d(&tmB, B, K, N, ldb, BK, pair ? 128 : kBN) ||
+      (pair && !encode_2d(&tmB64, B, K, N, ldb, BK, 64)))
     return FP8LA_ERR_CUDA;
   unsigned *status = status_word_ptr();
   if (!status) return FP8LA_ERR_CUDA;
@@ -791,7 +838,7 @@ fp8la_status gemm_pertensor_impl(const uint8_t *A, int64_t lda,
   args.fmt_bits = fmt_bits;
   if (pair) {
     const int64_t tiles = ((M + P_BM - 1) / P_BM) * ((N + P_BN - 1) / P_BN);
-    return launch_gemm_pair<false>(tmA, tmB, args, tiles, s);
+    return launch_gemm_pair<false>(tmA, tmB, tmB64, args, tiles, s);
   }
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + kBN - 1) / kBN);
   return launch_gemm<false>(tmA, tmB, args, tiles, s);
@@ -890,7 +937,7 @@ extern "C" fp8la_status fp8_grouped_gemm(
   if (pair) {
     const int64_t tiles = ((m_capacity + P_BM - 1) / P_BM + num_groups) *
                           ((N + P_BN - 1) / P_BN);
-    return launch_gemm_pair<true>(tmA, tmB, args, tiles, s);
+    return launch_gemm_pair<true>(tmA, tmB, tmB, args, tiles, s);
   }
   const int64_t tiles =
       ((m_capacity + BM - 1) / BM + num_groups) * ((N + kBN - 1) / kBN);
