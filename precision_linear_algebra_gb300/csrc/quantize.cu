@@ -23,8 +23,16 @@
 namespace fp8la {
 namespace {
 
+// Grid of the per-tensor passes: two 512-thread blocks per SM.  The
+// register cap of the launch bounds (three blocks' worth, <= 40 registers a
+// thread) leaves room on every SM for one CTA of the persistent GEMM
+// (320 threads x 64 registers) beside the two blocks, so that the
+// quantisation of the next operands can run on the same SMs while a GEMM is
+// in flight on another stream.  Four blocks of 512 threads fill the
+// register file, and the GEMM then waits for the whole pass to finish.
 constexpr int kThreads = 512;
-constexpr int kBlocksPerSm = 4;
+constexpr int kBlocksPerSm = 2;
+constexpr int kMinBlocksBound = 3;
 // Bytes of x's tail that the amax pass asks L2 to keep for the cast pass
 // (L2 is 129 MB; the rest of it holds the codes being written and other
 // work's data).
@@ -144,7 +152,7 @@ __device__ __forceinline__ float4 ld_hint4(const float4 *p, uint64_t policy) {
 // L2 policy (the rest evict-first), so that the part of x the cast pass
 // reads first -- it walks the tensor backwards -- is still in L2.
 template <int VEC>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kMinBlocksBound)
     amax_kernel(const float *__restrict__ x, int64_t rows, int64_t upr,
                 int64_t ldx, bool contiguous, int64_t keep_from,
                 float *amax_out) {
@@ -185,7 +193,7 @@ __global__ void __launch_bounds__(kThreads)
 
 // ------------------------------------------------------------------- cast
 template <int VEC, int FMT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kMinBlocksBound)
     cast_kernel(const float *__restrict__ x, int64_t rows, int64_t upr,
                 int64_t ldx, uint8_t *__restrict__ q, int64_t ldq,
                 bool contiguous, const float *amax_in, float *scale_out) {
