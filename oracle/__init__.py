@@ -41,7 +41,7 @@ from .e4m3 import decode_code, decode, encode, E4M3_MAX, NAN_CODE
 from . import e5m2
 from .bf16 import bf16_rne, bf16_bits_to_float
 from .quantize import (amax_fp32, scales_from_amax, quantize_pertensor,
-                       quantize_blockwise_32x32)
+                       quantize_pertensor_delayed, quantize_blockwise_32x32)
 from .gemm import (gemm_pertensor, gemm_blockscaled_32x32, gemm_grouped,
                    bound_pertensor, bound_blockscaled_32x32)
 

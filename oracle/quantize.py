@@ -16,6 +16,14 @@ The steps, in the order the method takes them:
    If amax == 0 or qscale is not finite, qscale = scale = 1.
 3. q_i = E4M3_RNE_satfinite(fp32(x_i * qscale)): one fp32 multiply, then the
    saturating round-to-nearest-even encode.
+
+Delayed scaling (``quantize_pertensor_delayed``) is a reading of ours, not a
+step the pages describe: it takes steps 2 and 3 with an amax carried over
+from an earlier call (the previous training or inference step) in place of
+step 1's, and performs step 1 on the current tensor only to record its amax
+for the next call.  The pages' remark that per-tensor scaling keeps values
+inside E4M3's +-448 then holds only up to the saturation of step 3: values
+beyond the carried-over amax land on the largest code.
 """
 
 import numpy as np
@@ -63,6 +71,21 @@ def quantize_pertensor(x, fmt="e4m3"):
     with np.errstate(over="ignore", invalid="ignore"):
         y = (x * qscale).astype(np.float32)      # fp32 * fp32 -> fp32, RNE
     return FORMATS[fmt][1](y), amax, scale
+
+
+def quantize_pertensor_delayed(x, amax_prev, fmt="e4m3"):
+    """Quantise with the scale of a carried-over amax (delayed scaling).
+
+    Steps 2 and 3 of the per-tensor scheme with ``amax_prev`` in place of the
+    tensor's own amax; step 1 on x gives the amax recorded for the next call.
+    Returns (codes uint8 with x's shape, amax of x fp32, scale fp32), where
+    scale = fp32(amax_prev / fmax) is the dequantisation factor of the codes.
+    """
+    x = np.asarray(x, dtype=np.float32)
+    qscale, scale = scales_from_amax(np.float32(amax_prev), fmt)
+    with np.errstate(over="ignore", invalid="ignore"):
+        y = (x * qscale).astype(np.float32)      # fp32 * fp32 -> fp32, RNE
+    return FORMATS[fmt][1](y), amax_fp32(x), scale
 
 
 def quantize_blockwise_32x32(x):
