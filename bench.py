@@ -42,6 +42,9 @@ GEMM_BYTES = 2 * N_SIZE * N_SIZE + 2 * N_SIZE * N_SIZE   # A, B codes + C bf16
 FP8_OVER_BF16 = 4.5 / 2.25        # nominal dense FP8 : BF16 tensor ratio
 WORKLOAD = ("per-tensor E4M3 quantize(A), quantize(B) + scaled GEMM, "
             "M=N=K=8192, A~N(0,1), B~N(0,0.02), 0.1% +-50sigma outliers, seed 0")
+WORKLOAD_DELAYED = ("per-tensor E4M3 delayed-scaling quantize(A), quantize(B) (scale from "
+                    "the amax recorded at the previous step, one pass) + scaled GEMM, "
+                    "M=N=K=8192, A~N(0,1), B~N(0,0.02), 0.1% +-50sigma outliers, seed 0")
 GEMM_SOURCES = ["precision_linear_algebra_gb300/csrc/gemm.cu",
                 "precision_linear_algebra_gb300/csrc/ptx.cuh"]
 QUANT_SOURCES = ["precision_linear_algebra_gb300/csrc/quantize.cu"]
@@ -259,7 +262,10 @@ class _Phases:
         return out
 
 
-def _workload_pertensor(fl, torch, dev, sptr, ph):
+def _workload_pertensor(fl, torch, dev, sptr, ph, delayed=False):
+    """The 8192^3 step.  delayed=True quantises each operand in one pass with
+    the scale of the amax it recorded at the previous step (delayed scaling);
+    the two amax words of each operand alternate between steps."""
     from precision_linear_algebra_gb300 import workloads
     A_np, B_np = workloads.square_outliers(N_SIZE, seed=0)
     A = torch.from_numpy(A_np).to(dev)
@@ -270,13 +276,32 @@ def _workload_pertensor(fl, torch, dev, sptr, ph):
     scale = torch.empty(2, dtype=torch.float32, device=dev)
     C = torch.empty((N_SIZE, N_SIZE), dtype=torch.bfloat16, device=dev)
     P = lambda t, i=0: t.data_ptr() + i * t.element_size()
+    # amax history for delayed scaling: hist[2 * operand + parity]
+    hist = torch.empty(4, dtype=torch.float32, device=dev)
+
+    def quant(x, q, amax_t, amax_i, scale_t, scale_i, s, operand, parity):
+        if delayed:
+            fl.fp8_quantize_pertensor_delayed(
+                P(x), N_SIZE, N_SIZE, N_SIZE, P(q), N_SIZE, P(hist, 2 * operand + (parity ^ 1)),
+                P(hist, 2 * operand + parity), P(scale_t, scale_i), 0, s)
+        else:
+            fl.fp8_quantize_pertensor(P(x), N_SIZE, N_SIZE, N_SIZE, P(q), N_SIZE,
+                                      P(amax_t, amax_i), P(scale_t, scale_i), s)
+
+    if delayed:
+        # seed the history with the current amax of each operand
+        for operand, x in enumerate((A, B)):
+            for parity in (0, 1):
+                fl.fp8_quantize_pertensor(P(x), N_SIZE, N_SIZE, N_SIZE, P(qa), N_SIZE,
+                                          P(hist, 2 * operand + parity), P(scale, 0), sptr)
+    counter = [0]
 
     def step():
+        parity = counter[0] & 1
+        counter[0] += 1
         ph.mark("quant")
-        fl.fp8_quantize_pertensor(P(A), N_SIZE, N_SIZE, N_SIZE, P(qa), N_SIZE,
-                                  P(amax, 0), P(scale, 0), sptr)
-        fl.fp8_quantize_pertensor(P(B), N_SIZE, N_SIZE, N_SIZE, P(qb), N_SIZE,
-                                  P(amax, 1), P(scale, 1), sptr)
+        quant(A, qa, amax, 0, scale, 0, sptr, 0, parity)
+        quant(B, qb, amax, 1, scale, 1, sptr, 1, parity)
         ph.mark("quant")
         ph.mark("gemm")
         fl.fp8_gemm(P(qa), N_SIZE, P(qb), N_SIZE, P(C), N_SIZE, N_SIZE, N_SIZE, N_SIZE,
@@ -305,10 +330,8 @@ def _workload_pertensor(fl, torch, dev, sptr, ph):
     def pstep(i):
         b = i & 1
         sq.wait_event(gdone[b])
-        fl.fp8_quantize_pertensor(P(A), N_SIZE, N_SIZE, N_SIZE, P(qa2[b]), N_SIZE,
-                                  P(amax2, 2 * b), P(scale2, 2 * b), sq.cuda_stream)
-        fl.fp8_quantize_pertensor(P(B), N_SIZE, N_SIZE, N_SIZE, P(qb2[b]), N_SIZE,
-                                  P(amax2, 2 * b + 1), P(scale2, 2 * b + 1), sq.cuda_stream)
+        quant(A, qa2[b], amax2, 2 * b, scale2, 2 * b, sq.cuda_stream, 0, b)
+        quant(B, qb2[b], amax2, 2 * b + 1, scale2, 2 * b + 1, sq.cuda_stream, 1, b)
         qdone[b].record(sq)
         sg.wait_event(qdone[b])
         fl.fp8_gemm(P(qa2[b]), N_SIZE, P(qb2[b]), N_SIZE, P(C), N_SIZE, N_SIZE, N_SIZE,
@@ -361,10 +384,8 @@ def _workload_pertensor(fl, torch, dev, sptr, ph):
         sq.wait_event(ev_a)
         sq.wait_event(ev_b)
         sq.wait_event(gdone[b])
-        fl.fp8_quantize_pertensor(P(E["A"][b]), N_SIZE, N_SIZE, N_SIZE, P(qa2[b]), N_SIZE,
-                                  P(amax2, 2 * b), P(scale2, 2 * b), sq.cuda_stream)
-        fl.fp8_quantize_pertensor(P(E["B"][b]), N_SIZE, N_SIZE, N_SIZE, P(qb2[b]), N_SIZE,
-                                  P(amax2, 2 * b + 1), P(scale2, 2 * b + 1), sq.cuda_stream)
+        quant(E["A"][b], qa2[b], amax2, 2 * b, scale2, 2 * b, sq.cuda_stream, 0, b)
+        quant(E["B"][b], qb2[b], amax2, 2 * b + 1, scale2, 2 * b + 1, sq.cuda_stream, 1, b)
         E["quantized"][b].record(sq)
         qdone[b].record(sq)
         # GEMM into C[b] once the D2H of step i-2 has drained it
@@ -385,14 +406,16 @@ def _workload_pertensor(fl, torch, dev, sptr, ph):
             main.wait_stream(st)
 
     return dict(step=step, pipeline=(pbegin, pstep, pend), e2e_pipeline=(ebegin, estep, eend),
-                flops=FLOPS, launches=5,
-                workload=WORKLOAD,
+                flops=FLOPS, launches=3 if delayed else 5,
+                workload=WORKLOAD_DELAYED if delayed else WORKLOAD,
+                quant_bytes_per_elem=5 if delayed else QUANT_BYTES_PER_ELEM,
                 config={"M": N_SIZE, "N": N_SIZE, "K": N_SIZE,
                         "l2": "inputs 2 x 268 MB fp32 > 129 MB L2; no flush"},
                 inputs=[(A, A_np), (B, B_np)], outputs=[C],
                 quant_elems=2 * N_SIZE * N_SIZE, gemm_label="gemm_e4m3_pair_kernel<false>",
                 gemm_bytes=GEMM_BYTES, profile=("gemm_e4m3_pertensor_8192", GEMM_SOURCES),
-                qprofile=("quantize_pertensor_8192", QUANT_SOURCES))
+                qprofile=(("quantize_pertensor_delayed_8192" if delayed
+                           else "quantize_pertensor_8192"), QUANT_SOURCES))
 
 
 def _workload_square(n):
@@ -489,7 +512,7 @@ def _workload_blockscaled(fl, torch, dev, sptr, ph, linears=("qkv", "attn_out", 
                                           sw.data_ptr(), sw.stride(0), sptr)
             ph.mark("gemm")
 
-    return dict(step=step, flops=flops, launches=12,
+    return dict(step=step, flops=flops, launches=12, quant_bytes_per_elem=5,
                 workload=("32x32 block-scaled E4M3: block-quantize activations [4096][K] ~ N(0,1) "
                           "and weights [N][K] ~ N(0,0.02), then the block-scaled GEMM, for the "
                           "four 70B-class linears qkv (10240,8192), attn_out (8192,8192), gate_up "
@@ -611,7 +634,10 @@ def _workload_attention(fl, torch, dev, sptr, ph, batch=2, heads=64, seq=2048, h
                 qprofile=("quantize_pertensor_8192", QUANT_SOURCES))
 
 
-WORKLOADS = {"pertensor8192": _workload_pertensor, "blockscaled": _workload_blockscaled,
+WORKLOADS = {"pertensor8192": _workload_pertensor,
+             "pertensor8192_delayed": (lambda fl, torch, dev, sptr, ph:
+                                       _workload_pertensor(fl, torch, dev, sptr, ph, delayed=True)),
+             "blockscaled": _workload_blockscaled,
              "grouped": _workload_grouped, "attention": _workload_attention,
              "square256": _workload_square(256),
              "square1024": _workload_square(1024)}
@@ -774,10 +800,9 @@ def run_gpu(args):
     g_avg = statistics.mean(g_ms)
     q_avg = statistics.mean(q_ms)
     gemm_tflops = W["flops"] / (g_avg * 1e-3) / 1e12
-    quant_gbs = (QUANT_BYTES_PER_ELEM * W["quant_elems"] / (q_avg * 1e-3) / 1e9
+    qbpe = W.get("quant_bytes_per_elem", QUANT_BYTES_PER_ELEM)
+    quant_gbs = (qbpe * W["quant_elems"] / (q_avg * 1e-3) / 1e9
                  if q_avg > 1e-6 else None)
-    if args.workload == "blockscaled":
-        quant_gbs = 5 * W["quant_elems"] / (q_avg * 1e-3) / 1e9   # one pass: 4 B read + 1 B written
     if args.workload == "attention":
         quant_gbs = None                                           # quantised at set-up
 
@@ -802,8 +827,7 @@ def run_gpu(args):
                                   "unit": "GB/s",
                                   "frac": quant_gbs / hbm if quant_gbs else None,
                                   "traffic": _profile_traffic(*W["qprofile"]),
-                                  "algorithmic_bytes_per_elem":
-                                      5 if args.workload == "blockscaled" else QUANT_BYTES_PER_ELEM},
+                                  "algorithmic_bytes_per_elem": qbpe},
             "breakdown": {"gemm_ms": g_avg, "quantize_ms": q_avg,
                           "gemm_tflops": gemm_tflops, "quantize_gbs": quant_gbs,
                           "schedule": ("cuda graph" if graph is not None else

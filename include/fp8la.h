@@ -117,6 +117,33 @@ FP8LA_API fp8la_status fp8_quantize_pertensor_ex(const float *x, int64_t rows,
                                                  fp8la_stream_t stream);
 
 /*
+ * Delayed-scaling per-tensor quantisation: one pass over x instead of two.
+ * The pages describe per-tensor scaling with the tensor's own amax
+ * ([P1] risks paragraph); this variant takes the scale from an amax
+ * carried over from an earlier call (typically the same tensor's amax at
+ * the previous step) and records the current amax for the next call:
+ *
+ *   qscale = fp32(fmax / amax_prev),  scale = fp32(amax_prev / fmax)
+ *            (amax_prev == 0 or qscale not finite: qscale = scale = 1)
+ *   q[i][j] = code of fp32(x[i][j] * qscale), RNE, saturating to +-fmax
+ *             (values beyond amax_prev land on the largest code)
+ *   amax_out = max |x[i][j]|, NaN ignored
+ *
+ * fmax = 448 (FP8LA_FORMAT_E4M3) or 57344 (FP8LA_FORMAT_E5M2).  x: fp32
+ * [rows][ldx] (device, read); q: uint8 [rows][ldq] (device, written);
+ * amax_prev: one fp32 (device, read); amax_out, scale_out: one fp32 each
+ * (device, written).  amax_prev, amax_out and scale_out must be three
+ * different words (FP8LA_ERR_INVALID_ARG otherwise): a caller keeping a
+ * history alternates two amax words between steps.  rows == 0 or cols == 0
+ * writes amax_out = 0 and the scale of amax_prev.  Memory traffic: 4 bytes
+ * read and 1 written per element.
+ */
+FP8LA_API fp8la_status fp8_quantize_pertensor_delayed(
+    const float *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q,
+    int64_t ldq, const float *amax_prev, float *amax_out, float *scale_out,
+    int32_t format, fp8la_stream_t stream);
+
+/*
  * 32x32 block E4M3 quantisation ([P3] implementation paragraph: scale
  * granularity of 32x32 blocks).  Each 32x32 tile (ragged at the right and
  * bottom edges: a tile covers only its in-range elements) is quantised

@@ -35,6 +35,8 @@ _S = ctypes.c_int
 SIGNATURES = [
     ("fp8_quantize_pertensor", _S, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P]),
     ("fp8_quantize_pertensor_ex", _S, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _I32, _P]),
+    ("fp8_quantize_pertensor_delayed", _S,
+     [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _I32, _P]),
     ("fp8_quantize_blockwise_32x32", _S, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P]),
     ("fp8_gemm", _S, [_P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P, _P]),
     ("fp8_gemm_ex", _S, [_P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P, _I32, _I32, _P]),
@@ -97,6 +99,12 @@ def _call(name, *args):
 def fp8_quantize_pertensor(x, rows, cols, ldx, q, ldq, amax_out, scale_out, stream):
     return _call("fp8_quantize_pertensor", x, rows, cols, ldx, q, ldq, amax_out,
                  scale_out, stream)
+
+
+def fp8_quantize_pertensor_delayed(x, rows, cols, ldx, q, ldq, amax_prev, amax_out, scale_out,
+                                   fmt, stream):
+    return _call("fp8_quantize_pertensor_delayed", x, rows, cols, ldx, q, ldq, amax_prev,
+                 amax_out, scale_out, fmt, stream)
 
 
 def fp8_quantize_pertensor_ex(x, rows, cols, ldx, q, ldq, amax_out, scale_out, fmt, stream):
@@ -191,6 +199,27 @@ def quantize_pertensor(x, q=None, amax=None, scale=None, fmt="e4m3"):
     scale = torch.empty(1, dtype=torch.float32, device=x.device) if scale is None else scale
     fp8_quantize_pertensor_ex(_ptr(x), rows, cols, _ld(x), _ptr(q), _ld(q),
                               _ptr(amax), _ptr(scale), _FORMATS[fmt], _stream())
+    return q, amax, scale
+
+
+def quantize_pertensor_delayed(x, amax_prev, q=None, amax=None, scale=None, fmt="e4m3"):
+    """One-pass quantisation with the scale of a carried-over amax.
+
+    x: fp32 CUDA [rows][cols]; amax_prev: fp32 CUDA tensor holding one value
+    (e.g. the amax this call returned at the previous step).  Returns
+    (q uint8 [rows][cols], amax fp32 [1] of x, scale fp32 [1] of the codes);
+    amax must not share storage with amax_prev.
+    """
+    import torch
+    assert x.dtype == torch.float32 and x.dim() == 2 and x.stride(1) == 1
+    rows, cols = x.shape
+    if q is None:
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    amax = torch.empty(1, dtype=torch.float32, device=x.device) if amax is None else amax
+    scale = torch.empty(1, dtype=torch.float32, device=x.device) if scale is None else scale
+    fp8_quantize_pertensor_delayed(_ptr(x), rows, cols, _ld(x), _ptr(q), _ld(q),
+                                   _ptr(amax_prev), _ptr(amax), _ptr(scale),
+                                   _FORMATS[fmt], _stream())
     return q, amax, scale
 
 

@@ -239,6 +239,65 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksBound)
   }
 }
 
+// ------------------------------------------------ delayed-scaling one pass
+// Codes with the scale of a carried-over amax (amax_prev), and this
+// tensor's own amax recorded in amax_out for the next call: one read of x
+// (4 B) and one write of codes (1 B) per element.
+template <int VEC, int FMT>
+__global__ void __launch_bounds__(kThreads, kMinBlocksBound)
+    delayed_kernel(const float *__restrict__ x, int64_t rows, int64_t upr,
+                   int64_t ldx, uint8_t *__restrict__ q, int64_t ldq,
+                   bool contiguous, const float *amax_prev, float *amax_out,
+                   float *scale_out) {
+  const Scales s = scales_from_amax<FMT>(*amax_prev);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *scale_out = s.scale;
+  const float qs = s.qscale;
+  const int64_t n = rows * upr;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  float m = 0.0f;
+  if (VEC == 4) {
+    if (contiguous) {
+      const float4 *x4 = reinterpret_cast<const float4 *>(x);
+      uint32_t *q4 = reinterpret_cast<uint32_t *>(q);
+      const uint64_t drop = policy_evict_first();
+      for (; i + 3 * stride < n; i += 4 * stride) {
+        const float4 a = ld_hint4(x4 + i, drop);
+        const float4 b = ld_hint4(x4 + i + stride, drop);
+        const float4 c = ld_hint4(x4 + i + 2 * stride, drop);
+        const float4 d = ld_hint4(x4 + i + 3 * stride, drop);
+        m = max_abs4(max_abs4(m, a), b);
+        m = max_abs4(max_abs4(m, c), d);
+        q4[i] = cvt4<FMT>(a, qs);
+        q4[i + stride] = cvt4<FMT>(b, qs);
+        q4[i + 2 * stride] = cvt4<FMT>(c, qs);
+        q4[i + 3 * stride] = cvt4<FMT>(d, qs);
+      }
+      for (; i < n; i += stride) {
+        const float4 v = ld_hint4(x4 + i, drop);
+        m = max_abs4(m, v);
+        q4[i] = cvt4<FMT>(v, qs);
+      }
+    } else {
+      for (; i < n; i += stride) {
+        const int64_t r = i / upr, c = i - r * upr;
+        const float4 v = ld_stream4(
+            reinterpret_cast<const float4 *>(x + r * ldx + c * 4));
+        m = max_abs4(m, v);
+        *reinterpret_cast<uint32_t *>(q + r * ldq + c * 4) = cvt4<FMT>(v, qs);
+      }
+    }
+  } else {
+    for (; i < n; i += stride) {
+      const int64_t r = i / upr, c = i - r * upr;
+      const float v = x[r * ldx + c];
+      m = fmaxf(m, fabsf(v));
+      q[r * ldq + c] = cvt1<FMT>(v, qs);
+    }
+  }
+  block_max_into(m, amax_out);
+}
+
 // --------------------------------------------------------- 32x32 block cast
 // One warp per 32x32 tile.  VEC = 4: lane l covers columns 4*(l%8)..+3 of
 // rows l/8, l/8+4, ..., l/8+28 with 16-byte loads; VEC = 1: lane l covers
@@ -369,6 +428,48 @@ fp8la_status quantize_pertensor_impl(const float *x, int64_t rows,
   return launch_status();
 }
 
+template <int FMT>
+fp8la_status quantize_delayed_impl(const float *x, int64_t rows, int64_t cols,
+                                   int64_t ldx, uint8_t *q, int64_t ldq,
+                                   const float *amax_prev, float *amax_out,
+                                   float *scale_out, cudaStream_t s) {
+  if (!amax_prev || !amax_out || !scale_out || rows < 0 || cols < 0)
+    return FP8LA_ERR_INVALID_ARG;
+  // Every block reads amax_prev while others update amax_out and block 0
+  // writes scale_out, so the three must be distinct words.
+  const void *a = amax_prev, *b = amax_out, *c = scale_out;
+  if (a == b || a == c || b == c) return FP8LA_ERR_INVALID_ARG;
+  const bool empty = rows == 0 || cols == 0;
+  if (!empty && (!x || !q || ldx < cols || ldq < cols))
+    return FP8LA_ERR_INVALID_ARG;
+  if (rows > (int64_t(1) << 40) || cols > (int64_t(1) << 40))
+    return FP8LA_ERR_UNSUPPORTED;
+  if (sm_count() <= 0) return FP8LA_ERR_CUDA;
+  if (cudaMemsetAsync(amax_out, 0, sizeof(float), s) != cudaSuccess)
+    return FP8LA_ERR_CUDA;
+  if (empty) {
+    delayed_kernel<1, FMT><<<1, 32, 0, s>>>(x, 0, 0, 0, q, 0, true, amax_prev,
+                                            amax_out, scale_out);
+    return launch_status();
+  }
+  const bool vec4 = cols % 4 == 0 && ldx % 4 == 0 && ldq % 4 == 0 &&
+                    aligned16(x) &&
+                    (reinterpret_cast<uintptr_t>(q) & 3u) == 0;
+  const bool contiguous = ldx == cols && ldq == cols;
+  if (vec4) {
+    const int64_t upr = cols / 4;
+    const int g = grid_for(rows * upr, kThreads);
+    delayed_kernel<4, FMT><<<g, kThreads, 0, s>>>(
+        x, rows, upr, ldx, q, ldq, contiguous, amax_prev, amax_out, scale_out);
+  } else {
+    const int g = grid_for(rows * cols, kThreads);
+    delayed_kernel<1, FMT><<<g, kThreads, 0, s>>>(
+        x, rows, cols, ldx, q, ldq, contiguous, amax_prev, amax_out,
+        scale_out);
+  }
+  return launch_status();
+}
+
 }  // namespace
 }  // namespace fp8la
 
@@ -420,4 +521,18 @@ extern "C" fp8la_status fp8_quantize_blockwise_32x32(
     block32_kernel<1><<<g, 256, 0, s>>>(x, rows, cols, ldx, q, ldq, scales,
                                         ld_scales, tiles_r, tiles_c);
   return launch_status();
+}
+
+extern "C" fp8la_status fp8_quantize_pertensor_delayed(
+    const float *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q,
+    int64_t ldq, const float *amax_prev, float *amax_out, float *scale_out,
+    int32_t format, fp8la_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (format == FP8LA_FORMAT_E4M3)
+    return quantize_delayed_impl<0>(x, rows, cols, ldx, q, ldq, amax_prev,
+                                    amax_out, scale_out, s);
+  if (format == FP8LA_FORMAT_E5M2)
+    return quantize_delayed_impl<1>(x, rows, cols, ldx, q, ldq, amax_prev,
+                                    amax_out, scale_out, s);
+  return FP8LA_ERR_INVALID_ARG;
 }

@@ -59,6 +59,13 @@ def test_host_argument_rejection(lib):
     assert lib.fp8_quantize_pertensor(one, -1, 4, 4, one, 4, one, one, None) == -1
     assert lib.fp8_quantize_pertensor(one, 4, 8, 4, one, 8, one, one, None) == -1
     assert lib.fp8_quantize_blockwise_32x32(one, 4, 64, 64, one, 64, one, 1, None) == -1
+    # delayed scaling: the carried-over amax, the new amax and the scale must
+    # be three different words; bad format
+    two, three = P(32), P(48)
+    assert lib.fp8_quantize_pertensor_delayed(one, 4, 4, 4, one, 4, two, two, three, 0, None) == -1
+    assert lib.fp8_quantize_pertensor_delayed(one, 4, 4, 4, one, 4, two, three, two, 0, None) == -1
+    assert lib.fp8_quantize_pertensor_delayed(one, 4, 4, 4, one, 4, None, two, three, 0, None) == -1
+    assert lib.fp8_quantize_pertensor_delayed(one, 4, 4, 4, one, 4, one, two, three, 7, None) == -1
     # gemm: negative sizes, ldc < N, lda < K, misaligned operands
     assert lib.fp8_gemm(one, 16, one, 16, one, 8, -1, 8, 16, one, one, None) == -1
     assert lib.fp8_gemm(one, 16, one, 16, one, 4, 8, 8, 16, one, one, None) == -1
