@@ -61,6 +61,7 @@ struct GemmArgs {
   uint64_t timeout_ns;
   int32_t withhold_first;  // diagnostic: skip the first TMA arrival
   int32_t c_vec16;         // C rows allow 16-byte stores (C 16-byte aligned, ldc % 8 == 0)
+  int32_t c_tma;           // CTA-pair kernel: C written through its tensor map
   uint32_t fmt_bits;       // operand-format bits of the MMA instruction descriptor
   int32_t split_tail;      // CTA-pair kernel: last tiles computed as two 128-column halves
 };
@@ -170,6 +171,45 @@ __device__ __forceinline__ void store_chunk32(uint32_t taddr, bool row_ok,
       if (n + j < N)
         crow[n + j] = static_cast<uint16_t>((j & 1) ? (w[j >> 1] >> 16)
                                                     : (w[j >> 1] & 0xFFFFu));
+  }
+}
+
+// As store_chunk32, for a whole 32 x 32 block through a TMA store: the warp
+// (lane = row) writes the block into the 2 KB shared buffer `stage` in the
+// 64-byte swizzled layout of the C tensor map (16-byte chunk q of row r at
+// r * 64 + 16 * (q ^ ((r >> 1) & 3)), which spreads each quarter-warp's
+// stores over all 32 banks), and lane 0 stores the box at (column n, row
+// row0).  Only blocks that lie inside C (and inside their group) come here;
+// edge blocks go through store_chunk32.  Lane 0 first waits until its
+// previous store has read the buffer.
+__device__ __forceinline__ void store_chunk32_tma(uint32_t taddr,
+                                                  uint32_t stage, int lane,
+                                                  const CUtensorMap *tmC,
+                                                  int n, int row0,
+                                                  float scale) {
+  uint32_t v[32];
+  tmem_ld32(taddr, v);
+  uint32_t w[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const __nv_bfloat162 h =
+        __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * j]), scale),
+                              __fmul_rn(__uint_as_float(v[2 * j + 1]), scale));
+    w[j] = *reinterpret_cast<const uint32_t *>(&h);
+  }
+  if (lane == 0) bulk_wait_read_all();
+  __syncwarp();
+  const uint32_t rowbase = stage + static_cast<uint32_t>(lane) * 64u;
+  const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+#pragma unroll
+  for (uint32_t q = 0; q < 4; ++q)
+    st_shared_v4(rowbase + 16u * (q ^ sw), w[4 * q], w[4 * q + 1],
+                 w[4 * q + 2], w[4 * q + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmC, stage, n, row0);
+    bulk_commit_group();
   }
 }
 
@@ -408,9 +448,16 @@ struct PairSmem {
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kPrefix = kMisc + 16;
   static constexpr int kEnd = kPrefix + (kMaxGroups + 1) * 4;
-  static constexpr int kAlloc = kEnd + 1024;
+  // One 2 KB staging buffer (32 rows x 32 BF16) per epilogue warp for the
+  // TMA-store epilogue, 1024-byte aligned for the 64-byte swizzle.
+  static constexpr int kCStage = (kEnd + 1023) / 1024 * 1024;
+  static constexpr int kCStageBytes = 32 * 32 * 2;
+  static constexpr int kAlloc = kCStage + P_EPI_WARPS * kCStageBytes + 1024;
 };
 
+static_assert(PairSmem::kCStage % 1024 == 0 &&
+                  PairSmem::kCStageBytes % 1024 == 0,
+              "C staging buffers");
 static_assert(PairSmem::kB % 1024 == 0 && PairSmem::kABytes % 1024 == 0 &&
                   PairSmem::kBBytes % 1024 == 0 && PairSmem::kBar % 8 == 0,
               "pair layout");
@@ -421,6 +468,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     gemm_e4m3_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmB64,
+                          const __grid_constant__ CUtensorMap tmC,
                           const GemmArgs a) {
   using L = PairSmem;
   constexpr int STAGES = P_STAGES;
@@ -605,6 +653,9 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     const uint32_t leader_tempty1 = mapa_shared(tempty_bar(1), 0);
     const int quarter = warp & 3;                 // TMEM lanes 32*quarter..
     const int col_half = warp >= 6 ? 1 : 0;       // which half of the columns
+    const uint32_t cstage = base + L::kCStage +
+                            static_cast<uint32_t>(warp < 4 ? warp : warp - 2) *
+                                L::kCStageBytes;
     for (int i = cluster_id; i < n_items; i += num_clusters, ++local) {
       int half;
       const TileInfo ti = item(i, half);
@@ -619,17 +670,34 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                                    a.status, abort_flag);
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after();
-      const int row =
-          ti.row0 + 128 * static_cast<int>(rank) + quarter * 32 + lane;
+      const int row_chunk0 =
+          ti.row0 + 128 * static_cast<int>(rank) + quarter * 32;
+      const int row = row_chunk0 + lane;
       const bool row_ok = row < ti.row_end;
       uint16_t *crow = a.C + static_cast<int64_t>(row) * a.ldc;
       const uint32_t taddr = tmem_base +
                              (static_cast<uint32_t>(quarter * 32) << 16) +
                              buf * P_BN + col0;
+      // Whole 32 x 32 blocks inside C (and inside the group) go out by TMA;
+      // blocks on an edge are stored row by row.
+      const bool rows_whole = a.c_tma != 0 && row_chunk0 + 32 <= ti.row_end;
+      if (rows_whole) {
 #pragma unroll 1
-      for (int c = 0; c < width; c += 32)
-        store_chunk32(taddr + c, row_ok, crow, ti.n0 + col0 + c, a.N, scale,
-                      a.c_vec16 != 0);
+        for (int c = 0; c < width; c += 32) {
+          const int n = ti.n0 + col0 + c;
+          if (n + 32 <= a.N)
+            store_chunk32_tma(taddr + c, cstage, lane, &tmC, n, row_chunk0,
+                              scale);
+          else
+            store_chunk32(taddr + c, true, crow, n, a.N, scale,
+                          a.c_vec16 != 0);
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < width; c += 32)
+          store_chunk32(taddr + c, row_ok, crow, ti.n0 + col0 + c, a.N, scale,
+                        a.c_vec16 != 0);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -639,6 +707,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           mbar_arrive_cluster(buf ? leader_tempty1 : leader_tempty0);
       }
     }
+    // C stores in flight finish before the CTA (and its shared memory) ends.
+    if (lane == 0) bulk_wait_all();
   }
 
   // ------------------------------------------------------------- teardown
@@ -727,10 +797,29 @@ fp8la_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB,
 
 // Launch the CTA-pair kernel on clusters of two CTAs, as many clusters as
 // can be resident at once (at most one per pair tile).
+// C as a BF16 tensor of `rows` x N with row stride ldc, stored in 32 x 32
+// boxes with the 64-byte swizzle (the layout store_chunk32_tma writes).
+bool encode_c(CUtensorMap *m, const uint16_t *C, int64_t ldc, int64_t rows,
+              int64_t N) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc) * 2};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+             const_cast<uint16_t *>(C), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool GROUPED>
 fp8la_status launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB,
-                              const CUtensorMap &tmB64, GemmArgs args,
-                              int64_t max_tiles, cudaStream_t s) {
+                              const CUtensorMap &tmB64, const CUtensorMap &tmC,
+                              GemmArgs args, int64_t max_tiles,
+                              cudaStream_t s) {
   using L = PairSmem;
   auto kern = gemm_e4m3_pair_kernel<GROUPED>;
   const int slot = GROUPED ? 3 : 2;
@@ -769,7 +858,8 @@ fp8la_status launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB,
   int64_t n = items < clusters ? items : clusters;
   if (n < 1) n = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * n), 1, 1);
-  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmB64, args) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmB64, tmC, args) !=
+      cudaSuccess)
     return FP8LA_ERR_CUDA;
   return launch_status();
 }
@@ -837,8 +927,13 @@ fp8la_status gemm_pertensor_impl(const uint8_t *A, int64_t lda,
   args.c_vec16 = aligned16(C) && ldc % 8 == 0;
   args.fmt_bits = fmt_bits;
   if (pair) {
+    CUtensorMap tmC{};
+    if (args.c_vec16) {
+      if (!encode_c(&tmC, C, ldc, M, N)) return FP8LA_ERR_CUDA;
+      args.c_tma = 1;
+    }
     const int64_t tiles = ((M + P_BM - 1) / P_BM) * ((N + P_BN - 1) / P_BN);
-    return launch_gemm_pair<false>(tmA, tmB, tmB64, args, tiles, s);
+    return launch_gemm_pair<false>(tmA, tmB, tmB64, tmC, args, tiles, s);
   }
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + kBN - 1) / kBN);
   return launch_gemm<false>(tmA, tmB, args, tiles, s);
@@ -935,9 +1030,14 @@ extern "C" fp8la_status fp8_grouped_gemm(
   // Upper bound on the tile count without reading m_offsets: each group
   // adds at most one partial row block.
   if (pair) {
+    CUtensorMap tmC{};
+    if (args.c_vec16) {
+      if (!encode_c(&tmC, C, ldc, m_capacity, N)) return FP8LA_ERR_CUDA;
+      args.c_tma = 1;
+    }
     const int64_t tiles = ((m_capacity + P_BM - 1) / P_BM + num_groups) *
                           ((N + P_BN - 1) / P_BN);
-    return launch_gemm_pair<true>(tmA, tmB, tmB, args, tiles, s);
+    return launch_gemm_pair<true>(tmA, tmB, tmB, tmC, args, tiles, s);
   }
   const int64_t tiles =
       ((m_capacity + BM - 1) / BM + num_groups) * ((N + kBN - 1) / kBN);
