@@ -33,6 +33,7 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kBlocksPerSm = 2;
 constexpr int kMinBlocksBound = 3;
+constexpr int kBlock32PerSm = 4;
 // Bytes of x's tail that the amax pass asks L2 to keep for the cast pass
 // (L2 is 129 MB; the rest of it holds the codes being written and other
 // work's data).
@@ -366,9 +367,11 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-int grid_for(int64_t units, int threads) {
+// Grid of a grid-stride launch: enough blocks for `units` threads' worth of
+// work, at most `per_sm` blocks per SM.
+int grid_for(int64_t units, int threads, int per_sm = kBlocksPerSm) {
   const int sms = sm_count();
-  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * kBlocksPerSm;
+  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * per_sm;
   int64_t g = (units + threads - 1) / threads;
   if (g > cap) g = cap;
   if (g < 1) g = 1;
@@ -513,7 +516,8 @@ extern "C" fp8la_status fp8_quantize_blockwise_32x32(
   const bool vec4 = cols % 4 == 0 && ldx % 4 == 0 && ldq % 4 == 0 &&
                     aligned16(x) &&
                     (reinterpret_cast<uintptr_t>(q) & 3u) == 0;
-  const int g = grid_for(tiles_r * tiles_c * 32, 256);
+  // 256-thread blocks of 64 registers: four per SM fill the register file.
+  const int g = grid_for(tiles_r * tiles_c * 32, 256, kBlock32PerSm);
   if (vec4)
     block32_kernel<4><<<g, 256, 0, s>>>(x, rows, cols, ldx, q, ldq, scales,
                                         ld_scales, tiles_r, tiles_c);
