@@ -89,6 +89,20 @@ def test_random_codes_random_scales(M, N, K):
     assert frac > 0.98
 
 
+def test_many_tiles_per_cta_all_outputs():
+    """About two 128 x 64 tiles per persistent CTA and a ragged last K stage
+    (K = 320: 10 scale blocks, 2.5 stages), every output checked: a scale
+    paired with the wrong K block after a tile change would show here."""
+    fl = lib()
+    M, N, K = 1536, 1600, 320
+    rng = np.random.default_rng(77)
+    A, B = random_codes(rng, (M, K)), random_codes(rng, (N, K))
+    sa, sb = _scales(rng, M, K), _scales(rng, N, K)
+    got = _run(fl, A, B, sa, sb)
+    frac = check_block(got, A, B, sa, sb, what="many tiles")
+    assert frac > 0.98
+
+
 def test_equal_scales_match_pertensor_bound():
     fl = lib()
     rng = np.random.default_rng(2)

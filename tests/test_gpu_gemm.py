@@ -70,6 +70,19 @@ def test_random_codes(M, N, K, variant):
     assert frac > 0.99
 
 
+def test_many_tiles_per_cta_all_outputs(variant):
+    """About two 256 x 256 tiles per CTA pair (4096 x 2560) with ragged N and
+    every output checked, so that tile changes, both TMEM accumulators and
+    the edge-block stores are all exercised."""
+    fl = lib()
+    rng = np.random.default_rng(99)
+    M, N, K = 4096, 2520, 256
+    A, B = random_codes(rng, (M, K)), random_codes(rng, (N, K))
+    got = _gemm(fl, A, B, np.float32(0.03125), np.float32(2.0), ldc_pad=8)
+    frac = check_pertensor(got, A, B, np.float32(0.03125), np.float32(2.0), what="many tiles")
+    assert frac > 0.98
+
+
 def test_identity_operand_selects_columns(variant):
     """A = I (code 0x38 = 1): C = dec(B)^T exactly (every E4M3 value is a bf16)."""
     fl = lib()
