@@ -418,12 +418,18 @@ def _workload_pertensor(fl, torch, dev, sptr, ph, delayed=False):
                            else "quantize_pertensor_8192"), QUANT_SOURCES))
 
 
+# Options of the square workloads (set from the command line).
+_SQUARE_OPTS = {"fmt": "e4m3", "gemm_variant": 0}
+_FMT_CODES = {"e4m3": 0, "e5m2": 1}
+
+
 def _workload_square(n):
     """Per-tensor quantize(A), quantize(B) + GEMM at M = N = K = n (N(0,1)
-    inputs).  These sizes are launch-bound, so the timed step replays one
-    CUDA graph holding the step's five launches."""
+    inputs), in the format --fmt.  The small sizes are launch-bound, so the
+    timed step replays one CUDA graph holding the step's launches."""
 
     def build(fl, torch, dev, sptr, ph):
+        f = _FMT_CODES[_SQUARE_OPTS["fmt"]]
         from precision_linear_algebra_gb300 import workloads
         A_np, B_np = workloads.square(n, seed=0)
         A = torch.from_numpy(A_np).to(dev)
@@ -435,21 +441,26 @@ def _workload_square(n):
         C = torch.empty((n, n), dtype=torch.bfloat16, device=dev)
         P = lambda t, i=0: t.data_ptr() + i * t.element_size()
 
+        def quant(stream_ptr):
+            fl.fp8_quantize_pertensor_ex(P(A), n, n, n, P(qa), n, P(amax, 0), P(scale, 0),
+                                         f, stream_ptr)
+            fl.fp8_quantize_pertensor_ex(P(B), n, n, n, P(qb), n, P(amax, 1), P(scale, 1),
+                                         f, stream_ptr)
+
+        def gemm(stream_ptr):
+            fl.fp8_gemm_ex(P(qa), n, P(qb), n, P(C), n, n, n, n, P(scale, 0), P(scale, 1),
+                           f, f, stream_ptr)
+
         def launches(stream_ptr):
-            fl.fp8_quantize_pertensor(P(A), n, n, n, P(qa), n, P(amax, 0), P(scale, 0),
-                                      stream_ptr)
-            fl.fp8_quantize_pertensor(P(B), n, n, n, P(qb), n, P(amax, 1), P(scale, 1),
-                                      stream_ptr)
-            fl.fp8_gemm(P(qa), n, P(qb), n, P(C), n, n, n, n, P(scale, 0), P(scale, 1),
-                        stream_ptr)
+            quant(stream_ptr)
+            gemm(stream_ptr)
 
         def step():
             ph.mark("quant")
-            fl.fp8_quantize_pertensor(P(A), n, n, n, P(qa), n, P(amax, 0), P(scale, 0), sptr)
-            fl.fp8_quantize_pertensor(P(B), n, n, n, P(qb), n, P(amax, 1), P(scale, 1), sptr)
+            quant(sptr)
             ph.mark("quant")
             ph.mark("gemm")
-            fl.fp8_gemm(P(qa), n, P(qb), n, P(C), n, n, n, n, P(scale, 0), P(scale, 1), sptr)
+            gemm(sptr)
             ph.mark("gemm")
 
         # One step captured as a CUDA graph (after a warm-up on a side stream,
@@ -465,12 +476,18 @@ def _workload_square(n):
             launches(cap.cuda_stream)
         torch.cuda.synchronize()
         return dict(step=step, graph=graph, flops=2.0 * n ** 3, launches=5,
-                    workload=("per-tensor E4M3 quantize(A), quantize(B) + scaled GEMM, "
-                              "M=N=K=%d, A, B ~ N(0,1), seed 0; one CUDA graph per step" % n),
-                    config={"M": n, "N": n, "K": n,
-                            "l2": "L2-resident inputs (%d KB fp32); no flush" % (8 * n * n // 1024)},
+                    workload=("per-tensor %s quantize(A), quantize(B) + scaled GEMM, "
+                              "M=N=K=%d, A, B ~ N(0,1), seed 0; one CUDA graph per step"
+                              % (_SQUARE_OPTS["fmt"].upper(), n)),
+                    config={"M": n, "N": n, "K": n, "format": _SQUARE_OPTS["fmt"],
+                            "gemm_variant": _SQUARE_OPTS["gemm_variant"],
+                            "l2": ("L2-resident inputs (%d KB fp32); no flush" % (8 * n * n // 1024)
+                                   if 8 * n * n < 64 << 20 else
+                                   "inputs 2 x %d MB fp32; no flush" % (4 * n * n >> 20))},
                     inputs=[(A, A_np), (B, B_np)], outputs=[C], quant_elems=2 * n * n,
-                    gemm_label="gemm_e4m3_pair_kernel<false>", gemm_bytes=4 * n * n,
+                    gemm_label=("gemm_e4m3_kernel<256,4,false>" if _SQUARE_OPTS["gemm_variant"] == 1
+                                else "gemm_e4m3_pair_kernel<false>"),
+                    gemm_bytes=4 * n * n,
                     profile=("gemm_e4m3_square_%d" % n, GEMM_SOURCES),
                     qprofile=("quantize_square_%d" % n, QUANT_SOURCES))
     return build
@@ -640,7 +657,8 @@ WORKLOADS = {"pertensor8192": _workload_pertensor,
              "blockscaled": _workload_blockscaled,
              "grouped": _workload_grouped, "attention": _workload_attention,
              "square256": _workload_square(256),
-             "square1024": _workload_square(1024)}
+             "square1024": _workload_square(1024),
+             "square4096": _workload_square(4096)}
 
 
 def run_gpu(args):
@@ -659,6 +677,9 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     fl.load()
+    _SQUARE_OPTS.update(fmt=args.fmt, gemm_variant=args.gemm_variant)
+    if args.workload.startswith("square") and args.gemm_variant:
+        fl.fp8la_set_gemm_variant(args.gemm_variant)
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
     ph = _Phases(torch, stream)
@@ -877,6 +898,10 @@ def main():
     ap.add_argument("--schedule", default="pipelined", choices=["pipelined", "serial"],
                     help="pipelined (default): step i+1's quantisation overlaps step i's GEMM "
                          "on a second stream; serial: one stream, steps back to back")
+    ap.add_argument("--fmt", default="e4m3", choices=sorted(_FMT_CODES),
+                    help="square* workloads: FP8 format of both operands")
+    ap.add_argument("--gemm-variant", type=int, default=0, choices=[0, 1, 2],
+                    help="square* workloads: GEMM kernel (0 by shape, 1 single CTA, 2 CTA pair)")
     ap.add_argument("--linears", default="",
                     help="blockscaled only: comma list of qkv,attn_out,gate_up,down "
                          "(default: all four)")
