@@ -56,6 +56,18 @@ def test_pertensor_ragged_and_strided(shape, ldx_pad, ldq_pad):
     _assert_same(_run_pertensor(fl, x, ldx_pad, ldq_pad), x)
 
 
+@pytest.mark.parametrize("shape", [(1, 4), (3, 4096), (512, 1024), (513, 1024), (1024, 1028)])
+def test_pertensor_one_launch_path_threshold(shape):
+    """Contiguous tensors of up to 512K floats take the one-launch cluster
+    path (no memset, amax exchanged through distributed shared memory);
+    larger ones the two-pass grid path.  Both sides of the size limit."""
+    fl = lib()
+    rng = np.random.default_rng(shape[0] * 31 + shape[1])
+    x = (rng.standard_normal(shape) * 7).astype(np.float32)
+    x.reshape(-1)[rng.integers(0, x.size)] = -1234.5     # the amax, negative
+    _assert_same(_run_pertensor(fl, x), x)
+
+
 def test_pertensor_special_values():
     fl = lib()
     x = np.array([[0.0, -0.0, np.nan, 1e-30, -1e-30, 3.0, -7.0, 2.0 ** -130, 448.0, -5.5]],
