@@ -299,6 +299,17 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksBound)
   block_max_into(m, amax_out);
 }
 
+// 32-bit load from the shared memory of a CTA of the cluster (cluster
+// address from mapa_shared).
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];"
+               : "=f"(v)
+               : "r"(cluster_addr)
+               : "memory");
+  return v;
+}
+
 // ------------------------------------------ small tensors: one launch
 // For a contiguous tensor of at most kSmallMaxUnits float4 units, where
 // launches rather than bytes set the time of the two-pass path, one
