@@ -402,7 +402,26 @@ __global__ void __launch_bounds__(256)
        t < tiles_r * tiles_c; t += warps_total) {
     const int64_t tr = t / tiles_c, tc = t - tr * tiles_c;
     const int64_t r0 = tr * 32, c0 = tc * 32;
-    if (VEC == 4) {
+    if (VEC == 4 && r0 + 32 <= rows && c0 + 32 <= cols) {
+      // Interior tile: no bounds checks, rows reached by a constant step.
+      const int64_t rstep = 4 * ldx;
+      const float *xp = x + (r0 + (lane >> 3)) * ldx + c0 + 4 * (lane & 7);
+      float4 v[8];
+      float m = 0.0f;
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        v[it] = ld_stream4(reinterpret_cast<const float4 *>(xp + it * rstep));
+        m = max_abs4(m, v[it]);
+      }
+      const float amax = warp_max(m);
+      const Scales s = scales_from_amax(amax);
+      if (lane == 0) scales[tr * ld_scales + tc] = s.scale;
+      const int64_t qstep = 4 * ldq;
+      uint8_t *qp = q + (r0 + (lane >> 3)) * ldq + c0 + 4 * (lane & 7);
+#pragma unroll
+      for (int it = 0; it < 8; ++it)
+        *reinterpret_cast<uint32_t *>(qp + it * qstep) = cvt4(v[it], s.qscale);
+    } else if (VEC == 4) {
       const int64_t col = c0 + 4 * (lane & 7);
       const bool col_ok = col < cols;
       float4 v[8];
