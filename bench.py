@@ -475,7 +475,10 @@ def _workload_square(n):
         with torch.cuda.graph(graph, stream=cap):
             launches(cap.cuda_stream)
         torch.cuda.synchronize()
-        return dict(step=step, graph=graph, flops=2.0 * n ** 3, launches=5,
+        # Kernels per step: tensors of at most 512K floats take the one-launch
+        # quantiser, larger ones amax + cast.
+        per_operand = 1 if n * n <= (1 << 19) else 2
+        return dict(step=step, graph=graph, flops=2.0 * n ** 3, launches=2 * per_operand + 1,
                     workload=("per-tensor %s quantize(A), quantize(B) + scaled GEMM, "
                               "M=N=K=%d, A, B ~ N(0,1), seed 0; one CUDA graph per step"
                               % (_SQUARE_OPTS["fmt"].upper(), n)),
