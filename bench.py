@@ -79,10 +79,15 @@ def _peaks():
 
 
 def _src_hash(paths):
+    """Hash of the sources' code: // comments and blank lines are left out,
+    so that an edit of comments alone does not retire a profile."""
     h = hashlib.sha256()
     for p in paths:
-        with open(os.path.join(ROOT, p), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, p), encoding="utf-8") as f:
+            for line in f:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode("utf-8") + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -428,6 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // complete on the leader's `full` barrier; the leader's commits are
 // multicast to both CTAs' `empty` / `tmem_full` barriers; both CTAs'
 // epilogue warps release an accumulator on the leader's `tmem_empty`.
+// The epilogue writes each whole 32 x 32 BF16 block of C through a 2 KB
+// shared-memory staging buffer per warp and one TMA store (store_chunk32_tma);
+// blocks on the edge of C, or of a group in the grouped GEMM, are stored
+// row by row (store_chunk32).
 constexpr int P_BM = 256;   // tile rows per CTA pair
 constexpr int P_BN = 256;   // tile columns per CTA pair
 constexpr int P_STAGES = 6;
