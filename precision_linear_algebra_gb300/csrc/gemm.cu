@@ -87,6 +87,9 @@ struct Smem {
 static_assert(Smem<256, 4>::kB % 1024 == 0 && Smem<256, 4>::kBBytes % 1024 == 0,
               "B tiles");
 static_assert(Smem<256, 4>::kAlloc <= 227 * 1024, "shared memory");
+static_assert(Smem<128, 6>::kB % 1024 == 0 && Smem<128, 6>::kBBytes % 1024 == 0,
+              "B tiles");
+static_assert(Smem<128, 6>::kAlloc <= 227 * 1024, "shared memory");
 
 // Tile t of a tiles_m x tiles_n grid in grouped order.
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n,
@@ -750,6 +753,10 @@ __global__ void zero_c_grouped_kernel(uint16_t *C, int64_t ldc,
 
 constexpr int kBN = 256;
 constexpr int kStages = 4;
+// 128 x 128 tiles for problems with few 256 x 256 tiles: more CTAs share the
+// work (1024^3: 64 CTAs instead of 16 pairs).
+constexpr int kSmallBN = 128;
+constexpr int kSmallStages = 6;
 
 bool encode_2d(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer,
                uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
@@ -780,13 +787,14 @@ bool encode_3d(CUtensorMap *m, const void *ptr, uint64_t d0, uint64_t d1,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool GROUPED>
+template <int TBN, int TSTAGES, bool GROUPED>
 fp8la_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB,
                          const GemmArgs &args, int64_t max_tiles,
                          cudaStream_t s) {
-  using L = Smem<kBN, kStages>;
-  auto kern = gemm_e4m3_kernel<kBN, kStages, GROUPED>;
-  if (once_per_device(GROUPED ? 1 : 0, [&] {
+  using L = Smem<TBN, TSTAGES>;
+  auto kern = gemm_e4m3_kernel<TBN, TSTAGES, GROUPED>;
+  const int slot = TBN == kSmallBN ? 5 : (GROUPED ? 1 : 0);
+  if (once_per_device(slot, [&] {
         return cudaFuncSetAttribute(
             kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
       }) != cudaSuccess)
@@ -799,8 +807,6 @@ fp8la_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB,
   return launch_status();
 }
 
-// Launch the CTA-pair kernel on clusters of two CTAs, as many clusters as
-// can be resident at once (at most one per pair tile).
 // C as a BF16 tensor of `rows` x N with row stride ldc, stored in 32 x 32
 // boxes with the 64-byte swizzle (the layout store_chunk32_tma writes).
 bool encode_c(CUtensorMap *m, const uint16_t *C, int64_t ldc, int64_t rows,
@@ -819,6 +825,8 @@ bool encode_c(CUtensorMap *m, const uint16_t *C, int64_t ldc, int64_t rows,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Launch the CTA-pair kernel on clusters of two CTAs, as many clusters as
+// can be resident at once (at most one per pair tile).
 template <bool GROUPED>
 fp8la_status launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB,
                               const CUtensorMap &tmB64, const CUtensorMap &tmC,
@@ -868,7 +876,8 @@ fp8la_status launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB,
   return launch_status();
 }
 
-// Kernel choice: 0 = by shape, 1 = single-CTA kernel, 2 = CTA-pair kernel.
+// Kernel choice: 0 = by shape, 1 = single-CTA kernel (128 x 256 tiles),
+// 2 = CTA-pair kernel, 3 = single-CTA kernel with 128 x 128 tiles.
 std::atomic<int> g_variant{0};
 
 fp8la_status check_operands(const uint8_t *A, int64_t lda, const uint8_t *B,
@@ -906,13 +915,19 @@ fp8la_status gemm_pertensor_impl(const uint8_t *A, int64_t lda,
     return launch_status();
   }
   // The CTA-pair kernel (256 x 256 tiles) unless the problem has too few
-  // rows to fill a pair tile, or the caller asked otherwise; the diagnostic
-  // path always uses the single-CTA kernel.
+  // rows to fill a pair tile, or so few pair tiles that they would leave
+  // three quarters of the SMs idle (then 128 x 128 single-CTA tiles), or the
+  // caller asked otherwise; the diagnostic path always uses the single-CTA
+  // 128 x 256 kernel.
   const int v = g_variant.load();
-  const bool pair = !withhold && (v == 2 || (v == 0 && M > BM));
+  const int sms = sm_count();
+  const int64_t pair_tiles = ((M + P_BM - 1) / P_BM) * ((N + P_BN - 1) / P_BN);
+  const bool small = !withhold &&
+                     (v == 3 || (v == 0 && sms > 0 && pair_tiles * 4 < sms));
+  const bool pair = !withhold && !small && (v == 2 || (v == 0 && M > BM));
   CUtensorMap tmA, tmB, tmB64;
   if (!encode_2d(&tmA, A, K, M, lda, BK, BM) ||
-      !encode_2d(&tmB, B, K, N, ldb, BK, pair ? 128 : kBN) ||
+      !encode_2d(&tmB, B, K, N, ldb, BK, pair || small ? 128 : kBN) ||
       (pair && !encode_2d(&tmB64, B, K, N, ldb, BK, 64)))
     return FP8LA_ERR_CUDA;
   unsigned *status = status_word_ptr();
@@ -939,8 +954,12 @@ fp8la_status gemm_pertensor_impl(const uint8_t *A, int64_t lda,
     const int64_t tiles = ((M + P_BM - 1) / P_BM) * ((N + P_BN - 1) / P_BN);
     return launch_gemm_pair<false>(tmA, tmB, tmB64, tmC, args, tiles, s);
   }
+  if (small) {
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + kSmallBN - 1) / kSmallBN);
+    return launch_gemm<kSmallBN, kSmallStages, false>(tmA, tmB, args, tiles, s);
+  }
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + kBN - 1) / kBN);
-  return launch_gemm<false>(tmA, tmB, args, tiles, s);
+  return launch_gemm<kBN, kStages, false>(tmA, tmB, args, tiles, s);
 }
 
 }  // namespace
@@ -1009,7 +1028,7 @@ extern "C" fp8la_status fp8_grouped_gemm(
     return b_group_stride % 16 != 0 ? FP8LA_ERR_ALIGNMENT
                                     : FP8LA_ERR_INVALID_ARG;
   // CTA pairs when groups average at least one pair tile of rows.
-  const int v = g_variant.load();
+  const int v = g_variant.load() == 3 ? 0 : g_variant.load();
   const bool pair = v == 2 || (v == 0 && m_capacity >= int64_t(P_BM) * num_groups);
   CUtensorMap tmA, tmB;
   if (!encode_2d(&tmA, A, K, m_capacity, lda, BK, BM) ||
@@ -1045,11 +1064,11 @@ extern "C" fp8la_status fp8_grouped_gemm(
   }
   const int64_t tiles =
       ((m_capacity + BM - 1) / BM + num_groups) * ((N + kBN - 1) / kBN);
-  return launch_gemm<true>(tmA, tmB, args, tiles, s);
+  return launch_gemm<kBN, kStages, true>(tmA, tmB, args, tiles, s);
 }
 
 extern "C" fp8la_status fp8la_set_gemm_variant(int32_t variant) {
-  if (variant < 0 || variant > 2) return FP8LA_ERR_INVALID_ARG;
+  if (variant < 0 || variant > 3) return FP8LA_ERR_INVALID_ARG;
   g_variant.store(variant);
   return FP8LA_OK;
 }

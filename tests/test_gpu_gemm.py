@@ -15,9 +15,10 @@ from precision_linear_algebra_gb300 import workloads
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=[1, 2], ids=["single_cta", "cta_pair"])
+@pytest.fixture(params=[1, 2, 3], ids=["single_cta", "cta_pair", "single_cta_128"])
 def variant(request):
-    """Run a test once per GEMM kernel (single-CTA and CTA-pair)."""
+    """Run a test once per GEMM kernel (single-CTA 128 x 256 tiles, CTA
+    pair, single-CTA 128 x 128 tiles)."""
     fl = lib()
     fl.fp8la_set_gemm_variant(request.param)
     yield request.param
