@@ -446,7 +446,6 @@ constexpr int P_EPI_WARPS = 8;
 struct PairSmem {
   static constexpr int kABytes = 128 * BK;   // this CTA's half of A
   static constexpr int kBBytes = 128 * BK;   // this CTA's half of B
-  static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * P_BN;
   static constexpr int kA = 0;
   static constexpr int kB = kA + P_STAGES * kABytes;
