@@ -229,6 +229,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // The grouped set-up reads m_offsets, so it waits for the previous
+  // kernel in the stream first (a no-op unless launched with programmatic
+  // stream serialization).
+  if (GROUPED) pdl_wait();
 
   const uint32_t bar0 = base + L::kBar;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -286,6 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The set-up above reads no input memory, so it may overlap the previous
+  // kernel in the stream; operands and scales are read only after this.
+  if (!GROUPED) pdl_wait();
   const uint32_t tmem_base = *tmem_slot;
   total_tiles = GROUPED ? pref[a.num_groups]
                         : ((a.M + BM - 1) / BM) * tiles_n;
@@ -485,6 +492,10 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // The grouped set-up reads m_offsets, so it waits for the previous
+  // kernel in the stream first (a no-op unless launched with programmatic
+  // stream serialization).
+  if (GROUPED) pdl_wait();
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
 
@@ -544,6 +555,9 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   __syncthreads();
   cluster_sync_all();  // peer barriers initialised before any remote use
   tc_fence_after();
+  // The set-up above reads no input memory, so it may overlap the previous
+  // kernel in the stream; operands and scales are read only after this.
+  if (!GROUPED) pdl_wait();
   const uint32_t tmem_base = *tmem_slot;
   const int total_tiles = GROUPED ? pref[a.num_groups]
                                   : ((a.M + P_BM - 1) / P_BM) * tiles_n;
@@ -802,7 +816,20 @@ fp8la_status launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB,
   if (sms <= 0) return FP8LA_ERR_CUDA;
   int64_t grid = max_tiles < sms ? max_tiles : sms;
   if (grid < 1) grid = 1;
-  kern<<<static_cast<int>(grid), kThreads, L::kAlloc, s>>>(tmA, tmB, args);
+  // Plain GEMMs start while the previous kernel in the stream finishes (the
+  // kernel waits for it before reading operands; see pdl_wait).
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = GROUPED ? 0 : 1;
+  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, args) != cudaSuccess)
+    return FP8LA_ERR_CUDA;
   return launch_status();
 }
 
@@ -869,6 +896,13 @@ fp8la_status launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB,
   int64_t n = items < clusters ? items : clusters;
   if (n < 1) n = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * n), 1, 1);
+  // Plain GEMMs start while the previous kernel in the stream finishes (the
+  // kernel waits for it before reading operands; see pdl_wait).
+  cudaLaunchAttribute attrs[2] = {attr[0], {}};
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = GROUPED ? 1 : 2;
   if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmB64, tmC, args) !=
       cudaSuccess)
     return FP8LA_ERR_CUDA;

@@ -165,6 +165,21 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a,
                : "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while its predecessor in the stream is still
+// running; pdl_wait() blocks until that predecessor has completed and its
+// memory operations are visible (it returns at once when there is none),
+// and must come before the first read of anything the predecessor may
+// write.  pdl_launch_dependents() lets the next kernel in the stream start
+// early (it changes nothing for a kernel launched normally).
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------- tcgen05
 // Tensor-memory allocation: executed by one whole warp.  The allocated base
 // address is written to shared memory at `dst_slot`.

@@ -199,6 +199,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksBound)
                 int64_t ldx, uint8_t *__restrict__ q, int64_t ldq,
                 bool contiguous, const float *amax_in, float *scale_out) {
   const Scales s = scales_from_amax<FMT>(*amax_in);
+  // A GEMM launched next may start its set-up now; it waits for this
+  // kernel to finish before reading the codes or the scale.
+  pdl_launch_dependents();
   if (blockIdx.x == 0 && threadIdx.x == 0) *scale_out = s.scale;
   const float qs = s.qscale;
   const int64_t n = rows * upr;
@@ -251,6 +254,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksBound)
                    bool contiguous, const float *amax_prev, float *amax_out,
                    float *scale_out) {
   const Scales s = scales_from_amax<FMT>(*amax_prev);
+  // A GEMM launched next may start its set-up now; it waits for this
+  // kernel to finish before reading the codes or the scale.
+  pdl_launch_dependents();
   if (blockIdx.x == 0 && threadIdx.x == 0) *scale_out = s.scale;
   const float qs = s.qscale;
   const int64_t n = rows * upr;
@@ -333,6 +339,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
                           uint32_t *__restrict__ q4, float *amax_out,
                           float *scale_out) {
   __shared__ float red[kSmallThreads / 32];
+  // A GEMM launched next may start its set-up now; it waits for this
+  // kernel to finish before reading the codes or the scale.
+  pdl_launch_dependents();
   __shared__ float cta_max;
   const uint32_t rank = cluster_ctarank();
   const int64_t stride = static_cast<int64_t>(kSmallCluster) * kSmallThreads;
