@@ -28,6 +28,15 @@
  *     error nothing is launched and a negative fp8la_status is returned.  A
  *     failed launch returns FP8LA_ERR_CUDA.  Nothing crosses the ABI as an
  *     exception, and no kernel traps.
+ *   - The first call of an entry point on a device does one-time set-up
+ *     (kernel attributes, occupancy queries); make it before capturing a
+ *     stream into a CUDA graph.  Later calls touch no CUDA runtime state
+ *     beyond their launches, so they can be captured.
+ *   - fp8_gemm launches with programmatic stream serialization: its set-up
+ *     (barriers, tensor memory) may overlap the previous kernel in the
+ *     stream, and it waits for that kernel to finish before reading any
+ *     operand or scale.  Ordering against other streams, copies and events
+ *     is unchanged.
  *   - Every wait inside a kernel is bounded in time.  A wait that runs out
  *     makes the kernel record FP8LA_ERR_DEVICE_TIMEOUT in a device status
  *     word and return early (its outputs are then undefined); read and clear
@@ -38,8 +47,9 @@
  *     ldc).  TMA needs 16-byte-aligned base pointers and strides: A and B
  *     must be 16-byte aligned with lda, ldb multiples of 16 (otherwise
  *     FP8LA_ERR_ALIGNMENT).  C needs only 2-byte alignment; when C is
- *     16-byte aligned and ldc is a multiple of 8 the kernels store 16-byte
- *     vectors, otherwise single elements.  M, N, K need not be multiples of any tile.
+ *     16-byte aligned and ldc is a multiple of 8 the kernels store whole
+ *     32 x 32 blocks by TMA and 16-byte vectors, otherwise single elements.
+ *     M, N, K need not be multiples of any tile.
  *     K = 0 writes C = 0; M = 0 or N = 0 does nothing.
  */
 #ifndef FP8LA_H
