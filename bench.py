@@ -38,7 +38,7 @@ METRIC = ("FP8 E4M3 GEMM TFLOP/s (% of GB300 dense FP8 peak) at 8192³; "
 N_SIZE = 8192
 FLOPS = 2.0 * N_SIZE ** 3
 QUANT_BYTES_PER_ELEM = 9          # amax pass reads 4 B, cast pass reads 4 B + writes 1 B
-E2E_REPEATS = 3                   # separate timed runs of the end-to-end loop (median reported)
+E2E_REPEATS = 5                   # separate timed runs of the end-to-end loop (median reported)
 GEMM_BYTES = 2 * N_SIZE * N_SIZE + 2 * N_SIZE * N_SIZE   # A, B codes + C bf16
 FP8_OVER_BF16 = 4.5 / 2.25        # nominal dense FP8 : BF16 tensor ratio
 WORKLOAD = ("per-tensor E4M3 quantize(A), quantize(B) + scaled GEMM, "
