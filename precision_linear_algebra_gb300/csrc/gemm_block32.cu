@@ -36,10 +36,12 @@
 //     FMAs (fma.rn.f32x2), two K blocks' partials per TMEM wait, each pair
 //     of K blocks in one asm statement.  After the last stage of a tile it
 //     rounds to BF16 and stores 64 bytes.
-//   * A stage is recycled only when its MMAs have completed and all eight
-//     promotion warps have read its scales (empty count 1 + 8); a
-//     partial-buffer set is reused once all eight warps hold its data in
-//     registers (pempty count 8).
+//   * A stage is recycled once all eight promotion warps have read its
+//     scales (empty count 8): they read them only after the stage's partial
+//     set is committed, which implies that the stage's MMAs, the last
+//     readers of its operand tiles, have completed.  A partial-buffer set is
+//     reused once all eight warps hold its data in registers (pempty count
+//     8).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -209,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1 + kPromoWarps);
+      mbar_init(empty_bar(s), kPromoWarps);
     }
     for (int p = 0; p < NSETS; ++p) {
       mbar_init(pfull_bar(p), 1);
@@ -295,8 +297,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < KPS; ++k)
             umma_f8f6f4(tmem_base + (set * KPS + k) * BN, adesc + 2u * k,
                         bdesc + 2u * k, idesc, 0u);
+          // No commit for the stage itself: its promotion warps release it
+          // after this set's commit, which implies these MMAs are done.
           umma_commit(pfull_bar(set));
-          umma_commit(empty_bar(s));
           if (++set == NSETS) { set = 0; sph ^= 1u; }
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
