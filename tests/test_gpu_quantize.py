@@ -98,11 +98,14 @@ def test_pertensor_8192_outliers_full_size():
         _assert_same(_run_pertensor(fl, x), x)
 
 
-def _sweep_chunk(fl, bits):
+def _sweep_chunk(fl, bits, vec4=True):
     """Quantise one chunk of fp32 bit patterns with 448 appended (so that
     chunks whose patterns stay within +-448 run with qscale == 1 and test the
-    cast alone) and compare with the oracle."""
-    x = np.concatenate([bits.view(np.float32), np.array([448.0], np.float32)])[None, :]
+    cast alone) and compare with the oracle.  vec4: pad the row to a multiple
+    of four values so that the 16-byte path (the one every aligned tensor
+    takes, with its paired conversions) runs; otherwise the scalar path."""
+    tail = [448.0, 0.0, 0.0, 0.0] if vec4 else [448.0]
+    x = np.concatenate([bits.view(np.float32), np.array(tail, np.float32)])[None, :]
     _assert_same(_run_pertensor(fl, x), x)
 
 
@@ -113,7 +116,8 @@ def test_cast_sweep_sampled():
     for top in (0x00, 0x3A, 0x3B, 0x3C, 0x3D, 0x43, 0x80, 0xBB, 0xC3, 0x7F, 0xFF):
         lo = np.uint64(top) << np.uint64(24)
         bits = (np.arange(1 << 24, dtype=np.uint64) + lo).astype(np.uint32)
-        _sweep_chunk(fl, bits)
+        _sweep_chunk(fl, bits, vec4=True)
+        _sweep_chunk(fl, bits, vec4=False)
     rng = np.random.default_rng(99)
     _sweep_chunk(fl, rng.integers(0, 2 ** 32, size=1 << 24, dtype=np.uint64).astype(np.uint32))
 
@@ -121,6 +125,8 @@ def test_cast_sweep_sampled():
 @pytest.mark.skipif(os.environ.get("FP8LA_EXHAUSTIVE") != "1",
                     reason="set FP8LA_EXHAUSTIVE=1 for the full 2^32 sweep")
 def test_cast_sweep_exhaustive():
+    """Every fp32 bit pattern through the 16-byte quantiser path, 2^24 at a
+    time (about ten minutes, most of it the oracle)."""
     fl = lib()
     for top in range(256):
         lo = np.uint64(top) << np.uint64(24)
