@@ -2,6 +2,8 @@
 bit against the oracle) and GEMMs with E5M2 operands, alone or mixed with
 E4M3 (within the same bound as the E4M3 GEMM)."""
 
+import os
+
 import numpy as np
 import pytest
 
@@ -46,14 +48,31 @@ def test_quantize_e5m2_specials():
     _assert_same(np.array([[np.inf, 2.0, -3.0, np.nan]], dtype=np.float32))
 
 
+def _sweep_chunk(bits, vec4=True):
+    """One chunk of fp32 bit patterns with 57344 appended (so that chunks
+    within +-57344 run with qscale == 1 and test the cast alone); vec4 pads
+    the row to a multiple of four values (the 16-byte path), else the scalar
+    path runs."""
+    tail = [57344.0, 0.0, 0.0, 0.0] if vec4 else [57344.0]
+    x = np.concatenate([bits.view(np.float32), np.array(tail, np.float32)])[None, :]
+    _assert_same(x)
+
+
 def test_cast_sweep_e5m2_sampled():
-    """Chunks of fp32 bit patterns with 57344 appended (so that chunks within
-    +-57344 run with qscale == 1 and test the cast alone)."""
     for top in (0x00, 0x37, 0x38, 0x46, 0x47, 0x80, 0xB8, 0xC7, 0x7F, 0xFF):
         lo = np.uint64(top) << np.uint64(24)
         bits = (np.arange(1 << 24, dtype=np.uint64) + lo).astype(np.uint32)
-        x = np.concatenate([bits.view(np.float32), np.array([57344.0], np.float32)])[None, :]
-        _assert_same(x)
+        _sweep_chunk(bits, vec4=True)
+        _sweep_chunk(bits, vec4=False)
+
+
+@pytest.mark.skipif(os.environ.get("FP8LA_EXHAUSTIVE") != "1",
+                    reason="set FP8LA_EXHAUSTIVE=1 for the full 2^32 sweep")
+def test_cast_sweep_e5m2_exhaustive():
+    """Every fp32 bit pattern through the 16-byte E5M2 quantiser path."""
+    for top in range(256):
+        lo = np.uint64(top) << np.uint64(24)
+        _sweep_chunk((np.arange(1 << 24, dtype=np.uint64) + lo).astype(np.uint32))
 
 
 @pytest.fixture(params=[1, 2], ids=["single_cta", "cta_pair"])
