@@ -222,26 +222,126 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def _cpu_baseline_subprocess():
+def _timed(f, *a, **k):
+    t0 = time.perf_counter()
+    out = f(*a, **k)
+    return out, time.perf_counter() - t0
+
+
+def _oracle_sample_workload(workload, linears=""):
+    """Time the oracle on a bounded sample of one step of `workload`; return
+    (estimated seconds for the full step, wall seconds timed, description).
+    Quantisation is scaled by element counts and GEMMs by output counts (the
+    oracle's cost per output is proportional to K)."""
+    import numpy as np
+    import oracle
+    from precision_linear_algebra_gb300 import workloads
+    if workload in ("pertensor8192", "pertensor8192_delayed"):
+        A, B = _oracle_inputs()
+        if workload == "pertensor8192":
+            est, wall = _oracle_sample(A, B, 4096, 1024, 4096)
+            return est, wall, ("oracle quantize of 4096 rows of A and of B + oracle GEMM of a "
+                               "1024 x 4096 output block of the 8192^3 workload")
+        rq, rg, cg = 4096, 1024, 4096
+        prev_a, prev_b = oracle.amax_fp32(A[:rq]), oracle.amax_fp32(B[:rq])
+        (qa, _, sa), t1 = _timed(oracle.quantize_pertensor_delayed, A[:rq], prev_a)
+        (qb, _, sb), t2 = _timed(oracle.quantize_pertensor_delayed, B[:rq], prev_b)
+        _, t3 = _timed(oracle.gemm_pertensor, qa, qb, sa, sb, rows=np.arange(rg) % rq,
+                       cols=np.arange(cg) % rq)
+        est = (t1 + t2) * (N_SIZE / rq) + t3 * (N_SIZE * N_SIZE / (rg * cg))
+        return est, t1 + t2 + t3, ("oracle delayed-scaling quantize of 4096 rows of A and of B "
+                                   "+ oracle GEMM of a 1024 x 4096 output block of the 8192^3 "
+                                   "workload")
+    if workload.startswith("square"):
+        n = int(workload[len("square"):])
+        A, B = workloads.square(n, seed=0)
+        rq = n if n <= 1024 else 2048
+        rg = n if n <= 1024 else 1024
+        fmt = _SQUARE_OPTS["fmt"]
+        (qa, _, sa), t1 = _timed(oracle.quantize_pertensor, A[:rq], fmt)
+        (qb, _, sb), t2 = _timed(oracle.quantize_pertensor, B, fmt)
+        _, t3 = _timed(oracle.gemm_pertensor, qa, qb, sa, sb, rows=np.arange(rg),
+                       a_fmt=fmt, b_fmt=fmt)
+        est = t1 * (n / rq) + t2 + t3 * (n / rg)
+        if rq == n and rg == n:
+            desc = "oracle quantize of A and B + oracle GEMM, the whole %d^3 step" % n
+        else:
+            desc = ("oracle quantize of %d rows of A and all of B + oracle GEMM of %d output "
+                    "rows (of %d)" % (rq, rg, n))
+        return est, t1 + t2 + t3, desc
+    if workload == "blockscaled":
+        names = linears.split(",") if linears else ["qkv", "attn_out", "gate_up", "down"]
+        est = wall = 0.0
+        for name in names:
+            X, W = workloads.transformer_linear(name, seed=0)
+            (M, K), N = X.shape, W.shape[0]
+            (qx, sx), t1 = _timed(oracle.quantize_blockwise_32x32, X[:1024])
+            (qw, sw), t2 = _timed(oracle.quantize_blockwise_32x32, W[:1024])
+            _, t3 = _timed(oracle.gemm_blockscaled_32x32, qx, qw, sx, sw,
+                           rows=np.arange(256), cols=np.arange(1024))
+            est += t1 * (M / 1024) + t2 * (N / 1024) + t3 * (M * N / (256 * 1024))
+            wall += t1 + t2 + t3
+            del X, W
+        return est, wall, ("per linear: oracle block quantize of 1024 rows of the activations "
+                           "and of the weights + oracle block-scaled GEMM of a 256 x 1024 output "
+                           "block (full K)")
+    if workload == "grouped":
+        counts, offs, X, W = workloads.moe_layer(seed=0)
+        E, N, K = W.shape
+        Mt = int(offs[-1])
+        (qx, _, sx), t1 = _timed(oracle.quantize_pertensor, X[:4096])
+        (qw, _, sw), t2 = _timed(oracle.quantize_pertensor, W[0][:4096])
+        _, t3 = _timed(oracle.gemm_pertensor, qx, qw, sx, sw, rows=np.arange(1024),
+                       cols=np.arange(4096))
+        est = (t1 + t2) * ((Mt * K + E * N * K) / (8192 * K)) + t3 * (Mt * N / (1024 * 4096))
+        return est, t1 + t2 + t3, ("oracle per-tensor quantize of 4096 activation rows and "
+                                   "4096 weight rows + oracle GEMM of a 1024 x 4096 output "
+                                   "block of expert 0 (K 4096)")
+    if workload == "attention":
+        batch, heads, seq, hd, sampled = 2, 64, 2048, 128, 16
+        E = batch * heads
+        g = np.random.default_rng(0)
+        wall = 0.0
+        for _ in range(sampled):
+            Q = workloads.normal(g, (seq, hd))
+            Kh = workloads.normal(g, (seq, hd))
+            P = g.random((seq, seq), dtype=np.float32) / np.float32(seq)
+            Vt = workloads.normal(g, (hd, seq))
+            qQ, _, sQ = oracle.quantize_pertensor(Q)
+            qK, _, sK = oracle.quantize_pertensor(Kh)
+            qP, _, sP = oracle.quantize_pertensor(P)
+            qV, _, sV = oracle.quantize_pertensor(Vt)
+            _, t1 = _timed(oracle.gemm_pertensor, qQ, qK, sQ, sK)
+            _, t2 = _timed(oracle.gemm_pertensor, qP, qV, sP, sV)
+            wall += t1 + t2
+        return wall * E / sampled, wall, (
+            "oracle GEMMs of %d heads (of %d): Q K^T (2048 x 2048, K 128) and P V (2048 x 128, "
+            "K 2048); set-up quantisation not timed" % (sampled, E))
+    raise ValueError(workload)
+
+
+def _cpu_baseline_subprocess(flops, workload="pertensor8192", linears=""):
     """The oracle on the host cores, run in a child process so that its BLAS
-    threads are set explicitly; about 10-30 s of CPU work."""
+    threads are set explicitly; about 10-30 s of CPU work on a sample of the
+    workload's step, scaled to the whole step."""
     threads = os.cpu_count() or 1
     env = dict(os.environ, OPENBLAS_NUM_THREADS=str(threads), OMP_NUM_THREADS=str(threads),
                MKL_NUM_THREADS=str(threads))
     code = ("import json,sys; sys.path.insert(0, %r); import bench; "
-            "A, B = bench._oracle_inputs(); "
-            "e, w = bench._oracle_sample(A, B, 1024, 256, 2048); print(json.dumps([e, w]))" % ROOT)
+            "bench._SQUARE_OPTS.update(fmt=%r); "
+            "e, w, d = bench._oracle_sample_workload(%r, %r); print(json.dumps([e, w, d]))"
+            % (ROOT, _SQUARE_OPTS["fmt"], workload, linears))
     try:
         out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True,
-                             text=True, timeout=300)
-        est, wall = json.loads(out.stdout.strip().splitlines()[-1])
+                             text=True, timeout=600)
+        est, wall, desc = json.loads(out.stdout.strip().splitlines()[-1])
     except Exception as exc:  # reported, not fatal
         return {"value": None, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                 "sample": "failed: %s" % exc}
-    return {"value": FLOPS / est / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": "oracle quantize of 1024 rows of A and of B + oracle GEMM of a 256 x 2048 "
-                      "output block of the 8192^3 workload (%.1f s wall), scaled to one full "
-                      "step by element and output counts" % wall}
+    return {"value": flops / est / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "ms_per_step": est * 1e3,
+            "sample": "%s (%.1f s wall), scaled to one full step by element and output counts"
+                      % (desc, wall)}
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -891,8 +991,9 @@ def run_gpu(args):
         }
         if args.workload != "pertensor8192":
             line["workload_kind"] = args.workload
-        if not args.no_cpu_baseline and args.workload == "pertensor8192":
-            line["cpu_baseline"] = _cpu_baseline_subprocess()
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = _cpu_baseline_subprocess(W["flops"], args.workload,
+                                                            args.linears)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
