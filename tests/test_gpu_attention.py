@@ -53,3 +53,44 @@ def test_scores_and_pv_per_head(H, S):
     sv = rng.uniform(0.01, 0.1, H).astype(np.float32)
     out = _grouped(fl, P, Vt, H, S, sp, sv)               # [H*S][D]
     _check(out, P, Vt, H, S, sp, sv)
+
+
+def _codes_fast(rng, shape):
+    """Uniform over the 254 finite E4M3 codes (all but 0x7F and 0xFF)."""
+    x = rng.integers(0, 254, size=shape, dtype=np.uint8)
+    return x + (x >= 0x7F).astype(np.uint8)
+
+
+def test_full_size_sampled():
+    """Batch 2 x 64 heads, sequence 2048, head_dim 128: both grouped GEMMs in
+    the launch configuration of the attention benchmark (one group per head,
+    128 groups of 2048 rows each), checked on sampled heads and rows against
+    the oracle (every column of the sampled rows)."""
+    import torch
+    fl = lib()
+    E, S, D = 128, 2048, 128
+    rng = np.random.default_rng(2048)
+    Q = _codes_fast(rng, (E * S, D))
+    Kt = _codes_fast(rng, (E, S, D))
+    P = _codes_fast(rng, (E * S, S))
+    Vt = _codes_fast(rng, (E, D, S))
+    sq, sk, sp, sv = (rng.uniform(0.001, 0.1, E).astype(np.float32) for _ in range(4))
+    offs = to_dev(np.arange(E + 1, dtype=np.int32) * S)
+    scores = fl.grouped_gemm(offs, to_dev(Q), to_dev(Kt), to_dev(sq), to_dev(sk))
+    out = fl.grouped_gemm(offs, to_dev(P), to_dev(Vt), to_dev(sp), to_dev(sv))
+    torch.cuda.synchronize()
+    assert fl.device_status() == 0
+    for e in (0, 37, 90, 127):
+        rows = np.sort(rng.choice(S, 24, replace=False))
+        g = torch.from_numpy(e * S + rows).cuda()
+        got_s = bf16_to_f64(scores.index_select(0, g))
+        got_o = bf16_to_f64(out.index_select(0, g))
+        A_s, A_o = Q[e * S:(e + 1) * S], P[e * S:(e + 1) * S]
+        for got, A, B, sa, sb in ((got_s, A_s, Kt[e], sq[e], sk[e]),
+                                  (got_o, A_o, Vt[e], sp[e], sv[e])):
+            r, _ = oracle.gemm_pertensor(A, B, sa, sb, rows=rows)
+            bound = oracle.bound_pertensor(r, A.shape[1], sa, sb,
+                                           np.abs(oracle.decode(A)).max(),
+                                           np.abs(oracle.decode(B)).max())
+            assert np.all(np.isfinite(got)), "head %d" % e
+            assert np.all(np.abs(got - r) <= bound), "head %d" % e
