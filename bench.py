@@ -5,7 +5,9 @@ fp32, N(0,1) with 0.1% +-50 sigma outliers) and B (N(0,0.02), same outlier
 rule) to E4M3 on the device (amax -> scale -> cast), then the scaled GEMM
 with FP32 accumulation and BF16 output.  Inputs are generated once (seeded),
 copied to HBM before timing.  `value` is 2*M*N*K / (time of one whole step),
-in TFLOP/s; the roofline object describes the GEMM kernel alone.  By default
+in TFLOP/s.  The roofline object describes the GEMM kernel: `achieved` from
+CUDA events around each GEMM launch over the timed steps, `achieved_isolated`
+from the same kernel timed one step at a time before them.  By default
 consecutive steps are pipelined: the HBM-bound quantisation of step i+1 runs
 on a second stream while the tensor-bound GEMM of step i runs (codes and
 scales double-buffered); every step still does all of its work, and the
@@ -369,10 +371,12 @@ class _Phases:
         self.events = []
         self.on = False
 
-    def mark(self, phase):
+    def mark(self, phase, stream=None):
+        """Record an event on `stream` (default: the launching stream); call
+        once before and once after the phase's launches."""
         if self.on:
             e = self.torch.cuda.Event(enable_timing=True)
-            e.record(self.stream)
+            e.record(self.stream if stream is None else stream)
             self.events.append((phase, e))
 
     def collect(self):
@@ -451,12 +455,16 @@ def _workload_pertensor(fl, torch, dev, sptr, ph, delayed=False):
     def pstep(i):
         b = i & 1
         sq.wait_event(gdone[b])
+        ph.mark("quant", sq)
         quant(A, qa2[b], amax2, 2 * b, scale2, 2 * b, sq.cuda_stream, 0, b)
         quant(B, qb2[b], amax2, 2 * b + 1, scale2, 2 * b + 1, sq.cuda_stream, 1, b)
+        ph.mark("quant", sq)
         qdone[b].record(sq)
         sg.wait_event(qdone[b])
+        ph.mark("gemm", sg)
         fl.fp8_gemm(P(qa2[b]), N_SIZE, P(qb2[b]), N_SIZE, P(C), N_SIZE, N_SIZE, N_SIZE,
                     N_SIZE, P(scale2, 2 * b), P(scale2, 2 * b + 1), sg.cuda_stream)
+        ph.mark("gemm", sg)
         gdone[b].record(sg)
 
     def pend():
@@ -863,6 +871,10 @@ def run_gpu(args):
             torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
+        # Every launch of the timed steps is bracketed by CUDA events on
+        # its own stream (not possible inside a replayed graph).
+        ph.events = []
+        ph.on = graph is None
         t0.record(stream)
         if graph is not None:
             for _ in range(args.steps):
@@ -878,18 +890,20 @@ def run_gpu(args):
                 step()
         t1.record(stream)
         torch.cuda.synchronize()
+        ph.on = False
         clocks = sampler.stop()
         if world > 1:
             dist.barrier()
-        return t0.elapsed_time(t1), serial_ms, clocks
+        phases = {k: v / args.steps for k, v in ph.collect().items()}
+        return t0.elapsed_time(t1), serial_ms, clocks, phases
 
-    ms_total, serial_ms, clocks = timed_region()
+    ms_total, serial_ms, clocks, phases = timed_region()
     # A run that saw a hardware or thermal slowdown, or SM clocks far below
     # their maximum with no reason given (a clock lock left by someone else),
     # is not a valid measurement: it is taken once more, and the line says so.
     if max_over_ranks(1.0 if _clocks_invalid(clocks) else 0.0, dev) > 0:
         first = clocks
-        ms_total, serial_ms, clocks = timed_region()
+        ms_total, serial_ms, clocks, phases = timed_region()
         clocks["remeasured"] = {"first_reasons": first["reasons"],
                                 "first_sm_mhz": first["sm_mhz"]}
     if fl.fp8_get_device_status(sptr) != 0:
@@ -960,15 +974,37 @@ def run_gpu(args):
 
     hbm, bf16_burst, bf16_sust, peak_src = _peaks()
     fp8_peak = bf16_burst * FP8_OVER_BF16
-    g_avg = statistics.mean(g_ms)
-    q_avg = statistics.mean(q_ms)
-    gemm_tflops = W["flops"] / (g_avg * 1e-3) / 1e12
-    gemm_gbs = W["gemm_bytes"] / (g_avg * 1e-3) / 1e9
+    # Kernel durations per step: over the timed steps from the events around
+    # each launch on its own stream; with a replayed graph (no events inside
+    # it) from the per-phase loop that ran before the timed region, which is
+    # also reported for every workload as the kernels' isolated timing.
+    g_iso = statistics.mean(g_ms)
+    q_iso = statistics.mean(q_ms)
+    if graph is None:
+        g_avg = phases.get("gemm", g_iso)
+        q_avg = phases.get("quant", q_iso)
+        timing = ("CUDA events around each launch, on its own stream, over the timed steps"
+                  + ("; pipelined, so each GEMM runs beside the next step's quantisation"
+                     if pipelined else ""))
+    else:
+        g_avg, q_avg = g_iso, q_iso
+        timing = ("CUDA events around each phase in a loop of single steps before the timed "
+                  "region (the timed steps replay one CUDA graph)")
     qbpe = W.get("quant_bytes_per_elem", QUANT_BYTES_PER_ELEM)
-    quant_gbs = (qbpe * W["quant_elems"] / (q_avg * 1e-3) / 1e9
-                 if q_avg > 1e-6 else None)
-    if args.workload == "attention":
-        quant_gbs = None                                           # quantised at set-up
+
+    def tflops(ms):
+        return W["flops"] / (ms * 1e-3) / 1e12
+
+    def gemm_gbs_of(ms):
+        return W["gemm_bytes"] / (ms * 1e-3) / 1e9
+
+    def quant_gbs_of(ms):
+        if args.workload == "attention" or ms <= 1e-6:
+            return None                                            # quantised at set-up
+        return qbpe * W["quant_elems"] / (ms * 1e-3) / 1e9
+
+    gemm_tflops, gemm_gbs, quant_gbs = tflops(g_avg), gemm_gbs_of(g_avg), quant_gbs_of(q_avg)
+    quant_gbs_iso = quant_gbs_of(q_iso)
 
     if rank == 0:
         line = {
@@ -982,26 +1018,34 @@ def run_gpu(args):
             "roofline": ({"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak,
                           "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak,
                           "traffic": _profile_traffic(*W["profile"]),
-                          "kernel": W["gemm_label"],
+                          "kernel": W["gemm_label"], "timing": timing,
                           "peak_source": "%s bf16 burst %.1f x nominal fp8/bf16 ratio 2"
                                          % (peak_src, bf16_burst),
                           "frac_of_sustained": (gemm_tflops / (bf16_sust * FP8_OVER_BF16)
-                                                if bf16_sust else None)}
+                                                if bf16_sust else None),
+                          "achieved_isolated": tflops(g_iso),
+                          "frac_isolated": tflops(g_iso) / fp8_peak}
                          if W.get("gemm_bound", "tensor") == "tensor" else
                          {"bound": "hbm", "achieved": gemm_gbs, "peak": hbm, "unit": "GB/s",
                           "frac": gemm_gbs / hbm,
                           "traffic": _profile_traffic(*W["profile"]),
-                          "kernel": W["gemm_label"],
+                          "kernel": W["gemm_label"], "timing": timing,
                           "algorithmic_bytes_per_step": W["gemm_bytes"],
                           "peak_source": "%s copy bandwidth" % peak_src,
                           "tflops": gemm_tflops,
-                          "frac_of_fp8_peak": gemm_tflops / fp8_peak}),
+                          "frac_of_fp8_peak": gemm_tflops / fp8_peak,
+                          "achieved_isolated": gemm_gbs_of(g_iso),
+                          "frac_isolated": gemm_gbs_of(g_iso) / hbm}),
             "roofline_quantize": {"bound": "hbm", "achieved": quant_gbs, "peak": hbm,
                                   "unit": "GB/s",
                                   "frac": quant_gbs / hbm if quant_gbs else None,
                                   "traffic": _profile_traffic(*W["qprofile"]),
-                                  "algorithmic_bytes_per_elem": qbpe},
+                                  "algorithmic_bytes_per_elem": qbpe, "timing": timing,
+                                  "achieved_isolated": quant_gbs_iso,
+                                  "frac_isolated": (quant_gbs_iso / hbm
+                                                    if quant_gbs_iso else None)},
             "breakdown": {"gemm_ms": g_avg, "quantize_ms": q_avg,
+                          "gemm_ms_isolated": g_iso, "quantize_ms_isolated": q_iso,
                           "gemm_tflops": gemm_tflops, "quantize_gbs": quant_gbs,
                           "schedule": ("cuda graph" if graph is not None else
                                        "pipelined" if pipelined else "serial"),
