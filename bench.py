@@ -160,6 +160,16 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def _median_min_per_step(xs, steps):
+    """[median, min] over the steps of the per-step sums of a phase's
+    consecutive interval durations (xs holds steps x k of them), or None."""
+    if not xs or steps <= 0 or len(xs) % steps:
+        return None
+    k = len(xs) // steps
+    per_step = [sum(xs[i * k:(i + 1) * k]) for i in range(steps)]
+    return [statistics.median(per_step), min(per_step)]
+
+
 _SLOWDOWNS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 
 
@@ -381,9 +391,16 @@ class _Phases:
 
     def collect(self):
         out = {}
-        for (ph, e0), (_, e1) in zip(self.events[0::2], self.events[1::2]):
-            out[ph] = out.get(ph, 0.0) + e0.elapsed_time(e1)
+        for ph, ds in self.durations().items():
+            out[ph] = sum(ds)
         self.events = []
+        return out
+
+    def durations(self):
+        """Each bracketed interval's duration (ms), per phase, in order."""
+        out = {}
+        for (ph, e0), (_, e1) in zip(self.events[0::2], self.events[1::2]):
+            out.setdefault(ph, []).append(e0.elapsed_time(e1))
         return out
 
 
@@ -894,7 +911,9 @@ def run_gpu(args):
         clocks = sampler.stop()
         if world > 1:
             dist.barrier()
+        per_launch = ph.durations()
         phases = {k: v / args.steps for k, v in ph.collect().items()}
+        phases["launches"] = per_launch
         return t0.elapsed_time(t1), serial_ms, clocks, phases
 
     ms_total, serial_ms, clocks, phases = timed_region()
@@ -1045,6 +1064,8 @@ def run_gpu(args):
                                   "frac_isolated": (quant_gbs_iso / hbm
                                                     if quant_gbs_iso else None)},
             "breakdown": {"gemm_ms": g_avg, "quantize_ms": q_avg,
+                          "gemm_ms_median_min": _median_min_per_step(
+                              phases.get("launches", {}).get("gemm"), args.steps),
                           "gemm_ms_isolated": g_iso, "quantize_ms_isolated": q_iso,
                           "gemm_tflops": gemm_tflops, "quantize_gbs": quant_gbs,
                           "schedule": ("cuda graph" if graph is not None else

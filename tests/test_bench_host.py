@@ -1,7 +1,7 @@
-"""The benchmark's validity rule for a timed region's clock record: a
-hardware or thermal slowdown, or SM clocks stuck far below their maximum
-with no reason active, make the run invalid (it is taken again); the power
-cap alone does not."""
+"""Host-side rules of the benchmark: a timed region whose clock record shows
+a hardware or thermal slowdown, or SM clocks stuck far below their maximum
+with no reason active, is invalid (it is taken again), while the power cap
+alone is not; and the per-step median and minimum of a kernel's times."""
 
 import os
 import sys
@@ -34,3 +34,10 @@ def test_low_clock_without_reason_is_a_lock():
 def test_no_samples_is_not_judged():
     assert not bench._clocks_invalid({"reasons": [], "sm_mhz": None, "sm_max_mhz": None,
                                       "samples": 0})
+
+
+def test_median_min_per_step():
+    xs = [1.0, 2.0, 3.0, 4.0, 5.0, 6.0]          # 3 steps x 2 launches
+    assert bench._median_min_per_step(xs, 3) == [7.0, 3.0]
+    assert bench._median_min_per_step([], 3) is None
+    assert bench._median_min_per_step([1.0, 2.0], 3) is None
