@@ -8,7 +8,12 @@
 // paragraph (one warp loads by TMA, one issues the MMA) and MoE paragraph
 // (grouped GEMM over experts).
 //
-// Design (sm_103a, one CTA per SM, persistent):
+// Two kernels live here.  The default for large problems is the CTA-pair
+// kernel further down (tcgen05 cta_group::2, 256 x 256 tiles per pair of
+// SMs; its own comment describes it).  The single-CTA kernel described next
+// serves small problems (128 x 128 tiles) and an explicit variant choice.
+//
+// Single-CTA design (sm_103a, one CTA per SM, persistent):
 //   * warp 4 (one lane): TMA producer.  For every 128-wide K block it loads
 //     a 128 x 128 A tile and a BN x 128 B tile (both K-major, 128-byte
 //     swizzle) into one stage of a STAGES-deep shared-memory ring, arming
