@@ -12,7 +12,7 @@
 //
 // The tile scales are arbitrary fp32 values, so they cannot be folded into
 // the tensor-core instruction; each 32-wide K block's product S_kb is formed
-// by one tcgen05.mma (M=128, N=128, K=32) into a fresh TMEM buffer and then
+// by one tcgen05.mma (M=128, N=64, K=32) into a fresh TMEM buffer and then
 // weighted and added on the CUDA cores.
 //
 // Design (one CTA per SM, persistent, 10 warps).  The promotion costs one

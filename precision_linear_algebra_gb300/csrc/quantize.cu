@@ -8,13 +8,17 @@
 // fp32(448/amax), scale = fp32(amax/448) (amax == 0 or qscale not finite:
 // both 1), q = E4M3 round-to-nearest-even saturating of fp32(x * qscale).
 //
-// Both kernels are HBM-bound streams.  The per-tensor path is two launches:
+// The kernels are HBM-bound streams.  The per-tensor path is two launches:
 // a 128-bit-load grid reduction whose blocks combine their maxima with one
 // atomicMax on the float's bit pattern (non-negative floats order like
 // their unsigned bit patterns; max is exact, so the result does not depend
 // on the order), then a cast pass that walks the tensor backwards so that
-// it starts on the part the reduction left in L2.  The block quantiser needs one pass: a
-// 32x32 fp32 tile (4 KB) fits one warp's registers.
+// it starts on the part the reduction left in L2.  Contiguous tensors of at
+// most 512K floats take one launch instead: one 16-CTA cluster does both
+// passes and combines the CTAs' maxima through distributed shared memory.
+// The block quantiser needs one pass: a 32x32 fp32 tile (4 KB) fits one
+// warp's registers.  Delayed scaling (the scale from a carried-over amax)
+// also needs one pass, which casts and records the new amax together.
 #include <cuda_fp8.h>
 
 #include "internal.h"
@@ -25,11 +29,11 @@ namespace {
 
 // Grid of the per-tensor passes: two 512-thread blocks per SM.  The
 // register cap of the launch bounds (three blocks' worth, <= 40 registers a
-// thread) leaves room on every SM for one CTA of the persistent GEMM
-// (320 threads x 64 registers) beside the two blocks, so that the
-// quantisation of the next operands can run on the same SMs while a GEMM is
-// in flight on another stream.  Four blocks of 512 threads fill the
-// register file, and the GEMM then waits for the whole pass to finish.
+// thread) leaves room on every SM for one CTA of the persistent GEMM (320
+// threads) beside at least one of the blocks, so that the quantisation of
+// the next operands can run on the same SMs while a GEMM is in flight on
+// another stream.  Four blocks of 512 threads fill the register file, and
+// the GEMM then waits for the whole pass to finish.
 constexpr int kThreads = 512;
 constexpr int kBlocksPerSm = 2;
 constexpr int kMinBlocksBound = 3;
