@@ -90,3 +90,33 @@ def test_host_argument_rejection(lib):
     # timeout setter
     assert lib.fp8la_set_wait_timeout_ns(10) == -1
     assert lib.fp8la_set_wait_timeout_ns(2_000_000_000) == 0
+
+
+def test_missing_library_fails_loudly():
+    import precision_linear_algebra_gb300 as fl
+    with pytest.raises(RuntimeError, match="not built"):
+        fl.load(os.path.join(ROOT, "no_such_dir", "libfp8la.so"))
+
+
+def test_no_cpu_fallback_without_a_gpu(lib):
+    """Without a GPU every compute entry point returns an error before any
+    launch and the binding raises; nothing is computed on the host."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: this checks the GPU-less behaviour")
+    import precision_linear_algebra_gb300 as fl
+    A = torch.zeros((32, 32), dtype=torch.uint8)
+    B = torch.zeros((32, 32), dtype=torch.uint8)
+    s = torch.ones(1)
+    C = torch.full((32, 32), 7.0, dtype=torch.bfloat16)
+    with pytest.raises(fl.Fp8laError) as e:
+        fl.fp8_gemm(A.data_ptr(), 32, B.data_ptr(), 32, C.data_ptr(), 32, 32, 32, 32,
+                    s.data_ptr(), s.data_ptr(), None)
+    assert e.value.status in (-3, -4)
+    assert torch.all(C == 7.0)
+    x = torch.ones((4, 4))
+    q = torch.zeros((4, 4), dtype=torch.uint8)
+    with pytest.raises(fl.Fp8laError):
+        fl.fp8_quantize_pertensor(x.data_ptr(), 4, 4, 4, q.data_ptr(), 4, s.data_ptr(),
+                                  s.data_ptr(), None)
+    assert torch.all(q == 0)
