@@ -171,3 +171,15 @@ def test_encode_pins_pass_on_oracle():
 @pytest.mark.parametrize("kind", ["ties_away", "no_saturation", "sign_of_zero_dropped"])
 def test_planted_encoder_mistakes_are_caught(kind):
     assert not _encode_pins_pass(_mutant(kind))
+
+
+def test_encode_is_monotone_and_odd():
+    """Rounding to the nearest code never reverses order, and enc(-x) is
+    enc(x) with the sign bit set: checked on sorted random fp32 values that
+    span the subnormals, every binade and the saturated range."""
+    rng = np.random.default_rng(7)
+    mags = np.exp2(rng.uniform(-14.0, 12.0, 200000)).astype(np.float32)
+    x = np.sort(mags)
+    vals = oracle.decode(oracle.encode(x))
+    assert np.all(np.diff(vals) >= 0)
+    assert np.array_equal(oracle.encode(-x), oracle.encode(x) | np.uint8(0x80))

@@ -102,3 +102,13 @@ def test_gemm_formats_exact_rational(fa, fb):
             q = Fraction(1, 8) * sum(dec[fa](int(A[m, k])) * dec[fb](int(B[n, k])) for k in range(K))
             # E5M2 sums may round in fp64 at 2^-53 relative
             assert abs(Fraction(float(r[m, n])) - q) <= abs(q) * Fraction(1, 2 ** 50)
+
+
+def test_encode_is_monotone_and_odd():
+    """As for E4M3: order-preserving and sign-symmetric rounding, over the
+    subnormals, every binade and the saturated range of E5M2."""
+    rng = np.random.default_rng(8)
+    x = np.sort(np.exp2(rng.uniform(-20.0, 18.0, 200000)).astype(np.float32))
+    vals = e5m2.decode(e5m2.encode(x))
+    assert np.all(np.diff(vals) >= 0)
+    assert np.array_equal(e5m2.encode(-x), e5m2.encode(x) | np.uint8(0x80))
