@@ -43,7 +43,9 @@ from .bf16 import bf16_rne, bf16_bits_to_float
 from .quantize import (amax_fp32, scales_from_amax, quantize_pertensor,
                        quantize_pertensor_delayed, quantize_blockwise_32x32)
 from .gemm import (gemm_pertensor, gemm_blockscaled_32x32, gemm_grouped,
-                   bound_pertensor, bound_blockscaled_32x32)
+                   bound_pertensor, bound_blockscaled_32x32, max_abs_decoded,
+                   max_abs_tile_scaled_32x32, tolerance_pertensor,
+                   tolerance_blockscaled_32x32)
 
 __all__ = [
     "decode_code", "decode", "encode", "E4M3_MAX", "NAN_CODE", "e5m2",
@@ -51,5 +53,7 @@ __all__ = [
     "amax_fp32", "scales_from_amax", "quantize_pertensor",
     "quantize_blockwise_32x32",
     "gemm_pertensor", "gemm_blockscaled_32x32", "gemm_grouped",
-    "bound_pertensor", "bound_blockscaled_32x32",
+    "bound_pertensor", "bound_blockscaled_32x32", "max_abs_decoded",
+    "max_abs_tile_scaled_32x32", "tolerance_pertensor",
+    "tolerance_blockscaled_32x32",
 ]

@@ -140,14 +140,48 @@ def gemm_grouped(A, m_offsets, B, scale_a, scale_b, cols=None):
     return r, C
 
 
+def max_abs_decoded(codes, fmt="e4m3"):
+    """max over the codes of |dec(code)|, NaN codes left out (0 if none).
+
+    This is the "max|a|" (or "max|b|") of the error bound below: a maximum
+    over the DECODED operand values, not over the raw byte codes.
+    """
+    d = np.abs(DECODERS[fmt](np.asarray(codes, dtype=np.uint8)))
+    d = d[~np.isnan(d)]
+    return float(d.max()) if d.size else 0.0
+
+
+def max_abs_tile_scaled_32x32(codes, s):
+    """max over (m, k) of |s[m//32, k//32] * dec(codes[m, k])| (NaN codes left out).
+
+    The block-scaled form of sa * max|a| in the error bound: each decoded
+    value is weighted by the scale of the 32x32 tile that holds it before the
+    maximum is taken.  Every product is exact in fp64 (a 24-bit scale times a
+    decoded value of at most 4 significant bits).
+    """
+    codes = np.asarray(codes, dtype=np.uint8)
+    s = np.asarray(s, dtype=np.float32).astype(np.float64)
+    M, K = codes.shape
+    best = 0.0
+    for r0 in range(0, M, 2048):                      # bounded memory
+        blk = np.abs(decode(codes[r0:r0 + 2048]))
+        rows = np.arange(r0, r0 + blk.shape[0]) // 32
+        cols = np.arange(K) // 32
+        w = np.abs(s[rows][:, cols]) * blk
+        w = w[~np.isnan(w)]
+        if w.size:
+            best = max(best, float(w.max()))
+    return best
+
+
 def bound_pertensor(r, K, scale_a, scale_b, max_a, max_b):
     """Allowed |C_gpu - C_ref| per element for a per-tensor GEMM.
 
     2^-8 * |C_ref| + 2^-22 * K * sa * sb * max|a| * max|b|, with a, b the
-    decoded E4M3 operand values and C_ref the exact product r.  The first term
-    is one bf16 rounding (unit roundoff 2^-8); the second covers an FP32
-    accumulation over K terms (4x the fp32 unit roundoff 2^-24 per term,
-    relative to the largest possible product).
+    decoded E4M3 operand values (``max_abs_decoded``) and C_ref the exact
+    product r.  The first term is one bf16 rounding (unit roundoff 2^-8); the
+    second covers an FP32 accumulation over K terms (4x the fp32 unit
+    roundoff 2^-24 per term, relative to the largest possible product).
     """
     return (2.0 ** -8) * np.abs(r) + (2.0 ** -22) * K * (
         float(np.float32(scale_a)) * float(np.float32(scale_b))
@@ -158,6 +192,25 @@ def bound_blockscaled_32x32(r, K, max_sa_a, max_sb_b):
     """The block-scaled form of ``bound_pertensor``.
 
     sa * max|a| is replaced by max over (m, k) of |sa[m//32, k//32] * dec(a)|
-    and likewise for B; the caller passes those two maxima.
+    and likewise for B (``max_abs_tile_scaled_32x32``); the caller passes
+    those two maxima.
     """
     return (2.0 ** -8) * np.abs(r) + (2.0 ** -22) * K * float(max_sa_a) * float(max_sb_b)
+
+
+def tolerance_pertensor(A, B, scale_a, scale_b, r, a_fmt="e4m3", b_fmt="e4m3"):
+    """The per-element bound for C = gemm_pertensor(A, B, scale_a, scale_b).
+
+    ``r`` is the oracle's exact product (for the whole matrix or any subset
+    of its elements); the maxima run over ALL of A and B.
+    """
+    K = np.asarray(A).shape[1]
+    return bound_pertensor(r, K, scale_a, scale_b,
+                           max_abs_decoded(A, a_fmt), max_abs_decoded(B, b_fmt))
+
+
+def tolerance_blockscaled_32x32(A, B, sa, sb, r):
+    """The per-element bound for C = gemm_blockscaled_32x32(A, B, sa, sb)."""
+    K = np.asarray(A).shape[1]
+    return bound_blockscaled_32x32(r, K, max_abs_tile_scaled_32x32(A, sa),
+                                   max_abs_tile_scaled_32x32(B, sb))

@@ -35,6 +35,22 @@ def random_codes(rng, shape):
     return rng.choice(FINITE_CODES, size=shape).astype(np.uint8)
 
 
+def assert_within_bound(C_gpu, r, bound, what=""):
+    """Assert |C_gpu - r| <= bound elementwise and that C_gpu is finite.
+
+    C_gpu, r, bound: numpy fp64 arrays of one shape (r the oracle's exact
+    product, bound from oracle.tolerance_*).  NaN or Inf in C_gpu fails.
+    """
+    assert np.all(np.isfinite(C_gpu)), what + ": non-finite output"
+    err = np.abs(C_gpu - r)
+    bad = ~(err <= bound)
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(
+            "%s: %d/%d outside bound; first at %s: got %r want %r (bound %r)"
+            % (what, bad.sum(), bad.size, i, C_gpu[i], r[i], bound[i]))
+
+
 def check_pertensor(C_gpu, A, B, sa, sb, rows=None, cols=None, what=""):
     """Assert the bound |C_gpu - r| <= 2^-8|r| + 2^-22 K sa sb max|a| max|b|.
 
@@ -46,15 +62,5 @@ def check_pertensor(C_gpu, A, B, sa, sb, rows=None, cols=None, what=""):
     if K == 0:
         assert np.all(C_gpu == 0), what
         return 1.0
-    maxa = np.abs(oracle.decode(A)).max()
-    maxb = np.abs(oracle.decode(B)).max()
-    bound = oracle.bound_pertensor(r, K, sa, sb, maxa, maxb)
-    assert np.all(np.isfinite(C_gpu)), what + ": non-finite output"
-    err = np.abs(C_gpu - r)
-    bad = err > bound
-    if bad.any():
-        i = np.argwhere(bad)[0]
-        raise AssertionError(
-            "%s: %d/%d outside bound; first at %s: got %r want %r (bound %r)"
-            % (what, bad.sum(), bad.size, tuple(i), C_gpu[tuple(i)], r[tuple(i)], bound[tuple(i)]))
+    assert_within_bound(C_gpu, r, oracle.tolerance_pertensor(A, B, sa, sb, r), what)
     return float(np.mean(C_gpu == oracle.bf16_bits_to_float(Cref)))

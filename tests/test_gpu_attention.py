@@ -31,8 +31,7 @@ def _check(got, A, B, E, m_per, sa, sb):
     for e in range(E):
         rows = slice(e * m_per, (e + 1) * m_per)
         r, Cref = oracle.gemm_pertensor(A[rows], B[e], sa[e], sb[e])
-        bound = oracle.bound_pertensor(r, K, sa[e], sb[e], np.abs(oracle.decode(A[rows])).max(),
-                                       np.abs(oracle.decode(B[e])).max())
+        bound = oracle.tolerance_pertensor(A[rows], B[e], sa[e], sb[e], r)
         assert np.all(np.abs(got[rows] - r) <= bound), "head %d" % e
 
 
@@ -89,8 +88,6 @@ def test_full_size_sampled():
         for got, A, B, sa, sb in ((got_s, A_s, Kt[e], sq[e], sk[e]),
                                   (got_o, A_o, Vt[e], sp[e], sv[e])):
             r, _ = oracle.gemm_pertensor(A, B, sa, sb, rows=rows)
-            bound = oracle.bound_pertensor(r, A.shape[1], sa, sb,
-                                           np.abs(oracle.decode(A)).max(),
-                                           np.abs(oracle.decode(B)).max())
+            bound = oracle.tolerance_pertensor(A, B, sa, sb, r)
             assert np.all(np.isfinite(got)), "head %d" % e
             assert np.all(np.abs(got - r) <= bound), "head %d" % e

@@ -15,7 +15,6 @@ pytestmark = pytest.mark.gpu
 
 FINITE = {"e4m3": np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8),
           "e5m2": np.array([c for c in range(256) if (c & 0x7C) != 0x7C], np.uint8)}
-DECODE = {"e4m3": oracle.decode, "e5m2": oracle.e5m2.decode}
 
 
 def _quantize(fl, x_np):
@@ -98,8 +97,7 @@ def test_gemm_formats(fa, fb, M, N, K, variant):
     assert fl.device_status() == 0
     got = bf16_to_f64(C)
     r, Cref = oracle.gemm_pertensor(A, B, sa, sb, a_fmt=fa, b_fmt=fb)
-    bound = oracle.bound_pertensor(r, K, sa, sb, np.abs(DECODE[fa](A)).max(),
-                                   np.abs(DECODE[fb](B)).max())
+    bound = oracle.tolerance_pertensor(A, B, sa, sb, r, a_fmt=fa, b_fmt=fb)
     assert np.all(np.isfinite(got))
     bad = np.abs(got - r) > bound
     assert not bad.any(), "%d outside the bound" % bad.sum()
@@ -118,6 +116,5 @@ def test_e5m2_end_to_end_quantize_gemm(variant):
     rqb, _, rsb = oracle.quantize_pertensor(B)
     assert np.array_equal(qa.cpu().numpy(), rqa) and np.array_equal(qb.cpu().numpy(), rqb)
     r, _ = oracle.gemm_pertensor(rqa, rqb, rsa, rsb, a_fmt="e5m2", b_fmt="e4m3")
-    bound = oracle.bound_pertensor(r, 512, rsa, rsb, np.abs(oracle.e5m2.decode(rqa)).max(),
-                                   np.abs(oracle.decode(rqb)).max())
+    bound = oracle.tolerance_pertensor(rqa, rqb, rsa, rsb, r, a_fmt="e5m2", b_fmt="e4m3")
     assert np.all(np.abs(bf16_to_f64(C) - r) <= bound)
