@@ -79,6 +79,8 @@ typedef int fp8la_status;
 #define FP8LA_ERR_UNSUPPORTED    -3  /* size beyond a TMA or kernel limit; no sm_10x GPU */
 #define FP8LA_ERR_CUDA           -4  /* a CUDA runtime or driver call failed */
 #define FP8LA_ERR_DEVICE_TIMEOUT -5  /* a bounded wait inside a kernel ran out */
+#define FP8LA_ERR_DEVICE_ARG     -6  /* a kernel found a device-side argument it
+                                        cannot use (fp8_grouped_gemm m_offsets) */
 
 /*
  * Per-tensor E4M3 quantisation ([P1] risks paragraph: E4M3 spans +-448 and
@@ -95,7 +97,9 @@ typedef int fp8la_status;
  * amax_out, scale_out: one fp32 each (device, written).  The scale stays on
  * the device so it can feed fp8_gemm by pointer with no host round trip.
  * Requires ldx >= cols, ldq >= cols.  rows == 0 or cols == 0 writes
- * amax = 0, scale = 1.  x and q must not overlap.
+ * amax = 0, scale = 1.  x and q must not overlap.  amax_out and scale_out
+ * must be two different words (the cast reads the amax while the scale is
+ * written): the same pointer for both returns FP8LA_ERR_INVALID_ARG.
  */
 FP8LA_API fp8la_status fp8_quantize_pertensor(const float *x, int64_t rows, int64_t cols,
                                     int64_t ldx, uint8_t *q, int64_t ldq,
@@ -234,9 +238,13 @@ FP8LA_API fp8la_status fp8_gemm_blockscaled_32x32(const uint8_t *A, int64_t lda,
  *
  * m_offsets: int32 [num_groups + 1] on the DEVICE, non-decreasing, starting
  * at 0, with m_offsets[num_groups] <= m_capacity; the host never reads it,
- * so routing results can feed the GEMM without a synchronisation.  A:
- * [m_capacity][lda]; C: [m_capacity][ldc]; rows at or past
- * m_offsets[num_groups] are neither read for any output nor written.
+ * so routing results can feed the GEMM without a synchronisation.  The
+ * kernels check it before computing anything: offsets that break these
+ * rules make the call write nothing to C and record FP8LA_ERR_DEVICE_ARG in
+ * the device status word (fp8_get_device_status), so a bad routing result
+ * cannot write outside C.  A: [m_capacity][lda]; C: [m_capacity][ldc];
+ * rows at or past m_offsets[num_groups] are neither read for any output nor
+ * written.
  * Groups with no rows are skipped.  scale_a, scale_b: fp32 [num_groups]
  * (device).  b_group_stride (elements) must be a multiple of 16 and
  * >= N * ldb.  1 <= num_groups <= 1024.
@@ -252,8 +260,9 @@ FP8LA_API fp8la_status fp8_grouped_gemm(int32_t num_groups, const int32_t *m_off
 /*
  * Synchronise `stream`, then read and clear the current device's status
  * word.  Returns FP8LA_OK, FP8LA_ERR_DEVICE_TIMEOUT if a kernel's bounded
- * wait ran out since the last call, or FP8LA_ERR_CUDA if the
- * synchronisation or the copy failed.
+ * wait ran out since the last call, FP8LA_ERR_DEVICE_ARG if a kernel
+ * refused a device-side argument (and no wait ran out), or FP8LA_ERR_CUDA if
+ * the synchronisation or the copy failed.
  */
 FP8LA_API fp8la_status fp8_get_device_status(fp8la_stream_t stream);
 
@@ -279,6 +288,26 @@ FP8LA_API fp8la_status fp8la_diag_gemm_withheld_arrival(const uint8_t *A, int64_
                                               const float *scale_a,
                                               const float *scale_b,
                                               fp8la_stream_t stream);
+
+/*
+ * Diagnostic, as fp8la_diag_gemm_withheld_arrival, for the other GEMM
+ * kernels.  kernel = FP8LA_DIAG_KERNEL_PAIR: the CTA-pair per-tensor kernel
+ * (as fp8_gemm with scale_a, scale_b one fp32 each; ld_sa, ld_sb ignored;
+ * M > 128), whose second CTA leaves out its first TMA loads, so the leader's
+ * MMA wait and then every wait of both CTAs run out.  kernel =
+ * FP8LA_DIAG_KERNEL_BLOCK32: the block-scaled kernel (arguments as
+ * fp8_gemm_blockscaled_32x32), whose producer leaves out its first stage.
+ * Either way the kernel records FP8LA_ERR_DEVICE_TIMEOUT, drains what it
+ * issued, frees its tensor memory and returns; C is undefined.  Other
+ * kernel values, or M, N, K <= 0, return FP8LA_ERR_INVALID_ARG.
+ */
+#define FP8LA_DIAG_KERNEL_PAIR 1
+#define FP8LA_DIAG_KERNEL_BLOCK32 2
+FP8LA_API fp8la_status fp8la_diag_withheld_arrival(
+    int32_t kernel, const uint8_t *A, int64_t lda, const uint8_t *B,
+    int64_t ldb, uint16_t *C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+    const float *scale_a, int64_t ld_sa, const float *scale_b, int64_t ld_sb,
+    fp8la_stream_t stream);
 
 /*
  * Choose the kernel behind fp8_gemm and fp8_grouped_gemm for calls made

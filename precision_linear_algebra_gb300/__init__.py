@@ -23,6 +23,7 @@ FP8LA_ERR_ALIGNMENT = -2
 FP8LA_ERR_UNSUPPORTED = -3
 FP8LA_ERR_CUDA = -4
 FP8LA_ERR_DEVICE_TIMEOUT = -5
+FP8LA_ERR_DEVICE_ARG = -6
 FP8LA_FORMAT_E4M3 = 0
 FP8LA_FORMAT_E5M2 = 1
 _FORMATS = {"e4m3": FP8LA_FORMAT_E4M3, "e5m2": FP8LA_FORMAT_E5M2}
@@ -47,6 +48,8 @@ SIGNATURES = [
     ("fp8_get_device_status", _S, [_P]),
     ("fp8la_set_wait_timeout_ns", _S, [_I64]),
     ("fp8la_diag_gemm_withheld_arrival", _S, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _P]),
+    ("fp8la_diag_withheld_arrival", _S,
+     [_I32, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _I64, _P, _I64, _P]),
     ("fp8la_set_gemm_variant", _S, [_I32]),
     ("fp8la_status_string", ctypes.c_char_p, [_S]),
     ("fp8la_version", _S, []),
@@ -150,6 +153,16 @@ def fp8la_set_wait_timeout_ns(ns):
 def fp8la_diag_gemm_withheld_arrival(A, lda, B, ldb, C, ldc, scale_a, scale_b, stream):
     return _call("fp8la_diag_gemm_withheld_arrival", A, lda, B, ldb, C, ldc,
                  scale_a, scale_b, stream)
+
+
+FP8LA_DIAG_KERNEL_PAIR = 1
+FP8LA_DIAG_KERNEL_BLOCK32 = 2
+
+
+def fp8la_diag_withheld_arrival(kernel, A, lda, B, ldb, C, ldc, M, N, K, scale_a, ld_sa,
+                                scale_b, ld_sb, stream):
+    return _call("fp8la_diag_withheld_arrival", kernel, A, lda, B, ldb, C, ldc, M, N, K,
+                 scale_a, ld_sa, scale_b, ld_sb, stream)
 
 
 def fp8la_set_gemm_variant(variant):

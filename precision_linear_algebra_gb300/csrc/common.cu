@@ -130,7 +130,9 @@ fp8la_status fp8_get_device_status(fp8la_stream_t stream) {
         cudaSuccess)
       return FP8LA_ERR_CUDA;
   }
-  return (v & fp8la::kStatusTimeout) ? FP8LA_ERR_DEVICE_TIMEOUT : FP8LA_OK;
+  if (v & fp8la::kStatusTimeout) return FP8LA_ERR_DEVICE_TIMEOUT;
+  if (v & fp8la::kStatusBadDeviceArg) return FP8LA_ERR_DEVICE_ARG;
+  return FP8LA_OK;
 }
 
 fp8la_status fp8la_set_wait_timeout_ns(int64_t timeout_ns) {
@@ -147,10 +149,26 @@ const char *fp8la_status_string(fp8la_status s) {
     case FP8LA_ERR_UNSUPPORTED: return "FP8LA_ERR_UNSUPPORTED";
     case FP8LA_ERR_CUDA: return "FP8LA_ERR_CUDA";
     case FP8LA_ERR_DEVICE_TIMEOUT: return "FP8LA_ERR_DEVICE_TIMEOUT";
+    case FP8LA_ERR_DEVICE_ARG: return "FP8LA_ERR_DEVICE_ARG";
     default: return "FP8LA_ERR_UNKNOWN";
   }
 }
 
-int fp8la_version(void) { return 100; }
+int fp8la_version(void) { return 101; }
+
+fp8la_status fp8la_diag_withheld_arrival(
+    int32_t kernel, const uint8_t *A, int64_t lda, const uint8_t *B,
+    int64_t ldb, uint16_t *C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+    const float *scale_a, int64_t ld_sa, const float *scale_b, int64_t ld_sb,
+    fp8la_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (kernel == FP8LA_DIAG_KERNEL_PAIR)
+    return fp8la::diag_pair_withheld(A, lda, B, ldb, C, ldc, M, N, K, scale_a,
+                                     scale_b, s);
+  if (kernel == FP8LA_DIAG_KERNEL_BLOCK32)
+    return fp8la::diag_block32_withheld(A, lda, B, ldb, C, ldc, M, N, K,
+                                        scale_a, ld_sa, scale_b, ld_sb, s);
+  return FP8LA_ERR_INVALID_ARG;
+}
 
 }  // extern "C"

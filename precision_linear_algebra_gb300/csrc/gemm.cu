@@ -64,7 +64,8 @@ struct GemmArgs {
   int32_t num_groups;        // grouped only
   unsigned *status;
   uint64_t timeout_ns;
-  int32_t withhold_first;  // diagnostic: skip the first TMA arrival
+  int32_t withhold_first;  // diagnostic: skip the first TMA arrival (CTA-pair
+                           // kernel: the second CTA's first loads)
   int32_t c_vec16;         // C rows allow 16-byte stores (C 16-byte aligned, ldc % 8 == 0)
   int32_t c_tma;           // CTA-pair kernel: C written through its tensor map
   uint32_t fmt_bits;       // operand-format bits of the MMA instruction descriptor
@@ -143,11 +144,40 @@ __device__ __forceinline__ TileInfo tile_info(int t, const GemmArgs &a,
     int mb, nb;
     tile_coords(t - pref[e], tiles_m, tiles_n, mb, nb);
     ti.row0 = m_lo + mb * TBM;
-    ti.row_end = m_hi;
+    ti.row_end = min(m_hi, a.M);   // m_offsets are checked at set-up as well
     ti.n0 = nb * BN;
     ti.group = e;
   }
   return ti;
+}
+
+// Grouped set-up, one warp: copy m_offsets to shared memory and build
+// pref[e] = number of tiles of groups 0..e-1 (TBM-row tiles, tiles_n column
+// tiles each).  Offsets that do not start at 0, decrease, or end past
+// m_capacity (a.M) leave pref[num_groups] = 0, so the CTA computes and
+// stores nothing, and the first CTA records kStatusBadDeviceArg.
+template <int TBM>
+__device__ __forceinline__ void load_group_offsets(const GemmArgs &a,
+                                                   int tiles_n,
+                                                   int32_t *offs_smem,
+                                                   int32_t *pref, int lane) {
+  for (int e = lane; e <= a.num_groups; e += 32) offs_smem[e] = a.m_offsets[e];
+  __syncwarp();
+  if (lane == 0) {
+    bool ok = offs_smem[0] == 0 && offs_smem[a.num_groups] <= a.M;
+    int acc = 0;
+    for (int e = 0; e < a.num_groups; ++e) {
+      pref[e] = acc;
+      const int me = offs_smem[e + 1] - offs_smem[e];
+      ok = ok && me >= 0;
+      acc += (me > 0 ? (me + TBM - 1) / TBM : 0) * tiles_n;
+    }
+    if (!ok) {
+      acc = 0;
+      if (blockIdx.x == 0) atomicOr(a.status, kStatusBadDeviceArg);
+    }
+    pref[a.num_groups] = acc;
+  }
 }
 
 // Epilogue of one accumulator row: 32 FP32 columns of TMEM -> x scale ->
@@ -276,22 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   int total_tiles;
-  if (GROUPED) {
-    // Per-group tile counts and their exclusive prefix sum (warp 0).
-    if (warp == 0) {
-      for (int e = lane; e <= a.num_groups; e += 32) offs_smem[e] = a.m_offsets[e];
-      __syncwarp();
-      if (lane == 0) {
-        int acc = 0;
-        for (int e = 0; e < a.num_groups; ++e) {
-          pref[e] = acc;
-          const int me = offs_smem[e + 1] - offs_smem[e];
-          acc += (me > 0 ? (me + BM - 1) / BM : 0) * tiles_n;
-        }
-        pref[a.num_groups] = acc;
-      }
-    }
-  }
+  if (GROUPED && warp == 0)
+    load_group_offsets<BM>(a, tiles_n, offs_smem, pref, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -543,19 +559,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     tmem_alloc_pair(smem_addr(tmem_slot), L::kTmemCols);
     tmem_relinquish_pair();
   }
-  if (GROUPED && warp == 0) {
-    for (int e = lane; e <= a.num_groups; e += 32) offs_smem[e] = a.m_offsets[e];
-    __syncwarp();
-    if (lane == 0) {
-      int acc = 0;
-      for (int e = 0; e < a.num_groups; ++e) {
-        pref[e] = acc;
-        const int me = offs_smem[e + 1] - offs_smem[e];
-        acc += (me > 0 ? (me + P_BM - 1) / P_BM : 0) * tiles_n;
-      }
-      pref[a.num_groups] = acc;
-    }
-  }
+  if (GROUPED && warp == 0)
+    load_group_offsets<P_BM>(a, tiles_n, offs_smem, pref, lane);
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();  // peer barriers initialised before any remote use
@@ -606,14 +611,18 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           }
           const uint32_t lf = mapa_shared(full_bar(s), 0);
           if (leader) mbar_arrive_expect_tx(full_bar(s), bytes);
-          tma_load_2d_pair(base + L::kA + s * L::kABytes, &tmA, lf, kb * BK,
-                           arow);
-          if (GROUPED)
-            tma_load_3d_pair(base + L::kB + s * L::kBBytes, &tmB, lf, kb * BK,
-                             brow, ti.group);
-          else
-            tma_load_2d_pair(base + L::kB + s * L::kBBytes,
-                             half < 0 ? &tmB : &tmB64, lf, kb * BK, brow);
+          // (Diagnostic only: the second CTA leaves out its first loads, so
+          // the leader's first stage never fills.)
+          if (!(a.withhold_first && !leader && issued == 0)) {
+            tma_load_2d_pair(base + L::kA + s * L::kABytes, &tmA, lf, kb * BK,
+                             arow);
+            if (GROUPED)
+              tma_load_3d_pair(base + L::kB + s * L::kBBytes, &tmB, lf,
+                               kb * BK, brow, ti.group);
+            else
+              tma_load_2d_pair(base + L::kB + s * L::kBBytes,
+                               half < 0 ? &tmB : &tmB64, lf, kb * BK, brow);
+          }
           ++issued;
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
@@ -756,10 +765,24 @@ __global__ void zero_c_kernel(uint16_t *C, int64_t ldc, int64_t M, int64_t N) {
   }
 }
 
-// Grouped variant of the K = 0 case: zero the rows each group owns.
+// Grouped variant of the K = 0 case: zero the rows each group owns, after
+// the same check of m_offsets as the GEMM kernels make (on failure nothing
+// is written and kStatusBadDeviceArg is recorded).
 __global__ void zero_c_grouped_kernel(uint16_t *C, int64_t ldc,
                                       const int32_t *m_offsets, int32_t E,
-                                      int64_t N) {
+                                      int64_t N, int64_t m_capacity,
+                                      unsigned *status) {
+  __shared__ int bad;
+  if (threadIdx.x == 0)
+    bad = m_offsets[0] != 0 || m_offsets[E] > m_capacity;
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (m_offsets[e + 1] < m_offsets[e]) bad = 1;
+  __syncthreads();
+  if (bad) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, kStatusBadDeviceArg);
+    return;
+  }
   const int64_t rows = m_offsets[E];
   const int64_t n = rows * N;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -955,14 +978,15 @@ fp8la_status gemm_pertensor_impl(const uint8_t *A, int64_t lda,
   // The CTA-pair kernel (256 x 256 tiles) unless the problem has too few
   // rows to fill a pair tile, or so few pair tiles that they would leave
   // three quarters of the SMs idle (then 128 x 128 single-CTA tiles), or the
-  // caller asked otherwise; the diagnostic path always uses the single-CTA
-  // 128 x 256 kernel.
+  // caller asked otherwise.  The diagnostic path uses the single-CTA 128 x 256
+  // kernel (withhold == 1) or the CTA-pair kernel (withhold == 2).
   const int v = g_variant.load();
   const int sms = sm_count();
   const int64_t pair_tiles = ((M + P_BM - 1) / P_BM) * ((N + P_BN - 1) / P_BN);
   const bool small = !withhold &&
                      (v == 3 || (v == 0 && sms > 0 && pair_tiles * 4 < sms));
-  const bool pair = !withhold && !small && (v == 2 || (v == 0 && M > BM));
+  const bool pair = withhold == 2 ||
+                    (!withhold && !small && (v == 2 || (v == 0 && M > BM)));
   CUtensorMap tmA, tmB, tmB64;
   if (!encode_2d(&tmA, A, K, M, lda, BK, BM) ||
       !encode_2d(&tmB, B, K, N, ldb, BK, pair || small ? 128 : kBN) ||
@@ -1042,6 +1066,20 @@ extern "C" fp8la_status fp8la_diag_gemm_withheld_arrival(
                              1);
 }
 
+namespace fp8la {
+// The CTA-pair kernel with the second CTA's first loads withheld (the
+// diagnostic entry point for the block-scaled kernel lives beside it).
+fp8la_status diag_pair_withheld(const uint8_t *A, int64_t lda, const uint8_t *B,
+                                int64_t ldb, uint16_t *C, int64_t ldc,
+                                int64_t M, int64_t N, int64_t K,
+                                const float *scale_a, const float *scale_b,
+                                cudaStream_t s) {
+  if (M <= BM || K <= 0) return FP8LA_ERR_INVALID_ARG;
+  return gemm_pertensor_impl(A, lda, B, ldb, C, ldc, M, N, K, scale_a, scale_b,
+                             s, 2);
+}
+}  // namespace fp8la
+
 extern "C" fp8la_status fp8_grouped_gemm(
     int32_t num_groups, const int32_t *m_offsets, int64_t m_capacity,
     const uint8_t *A, int64_t lda, const uint8_t *B, int64_t ldb,
@@ -1057,8 +1095,10 @@ extern "C" fp8la_status fp8_grouped_gemm(
   if (!device_is_sm10x()) return FP8LA_ERR_UNSUPPORTED;
   if (K == 0) {
     const int sms = sm_count();
+    unsigned *status = status_word_ptr();
+    if (!status) return FP8LA_ERR_CUDA;
     zero_c_grouped_kernel<<<sms > 0 ? sms * 4 : 1, 256, 0, s>>>(
-        C, ldc, m_offsets, num_groups, N);
+        C, ldc, m_offsets, num_groups, N, m_capacity, status);
     return launch_status();
   }
   if (!scale_a || !scale_b) return FP8LA_ERR_INVALID_ARG;

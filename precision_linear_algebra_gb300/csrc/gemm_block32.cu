@@ -75,6 +75,7 @@ struct BsArgs {
   unsigned *status;
   uint64_t timeout_ns;
   int32_t c_vec16;
+  int32_t withhold_first;  // diagnostic: skip the first stage's TMA arrival
 };
 
 struct Lay {
@@ -253,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // Operand tiles and the stage's scale boxes, all on one barrier.
         // TMA zero-fills scale entries past the grid's edge.
-        if (lane == 0) {
+        if (lane == 0 && !(a.withhold_first && issued == 0)) {
           const uint32_t fb = full_bar(s);
           const uint32_t sslot = base + Lay::kScale + s * Lay::kScaleSlot;
           mbar_arrive_expect_tx(fb, Lay::kStageBytes);
@@ -270,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t st = 0; st < STAGES; ++st) {
         if (issued <= st) break;
         const uint32_t arms = (issued - 1 - st) / STAGES + 1;
+        if (a.withhold_first && st == 0 && arms == 1) continue;  // never armed
         mbar_wait_drain(full_bar(st), (arms - 1) & 1u, a.timeout_ns, a.status);
       }
     }
@@ -439,15 +441,18 @@ bool encode_2d_bs(CUtensorMap *m, const void *ptr, uint64_t inner,
 
 using namespace fp8la;
 
-extern "C" fp8la_status fp8_gemm_blockscaled_32x32(
-    const uint8_t *A, int64_t lda, const uint8_t *B, int64_t ldb, uint16_t *C,
-    int64_t ldc, int64_t M, int64_t N, int64_t K, const float *sa,
-    int64_t ld_sa, const float *sb, int64_t ld_sb, fp8la_stream_t stream) {
+namespace fp8la {
+namespace {
+
+fp8la_status blockscaled_impl(const uint8_t *A, int64_t lda, const uint8_t *B,
+                              int64_t ldb, uint16_t *C, int64_t ldc, int64_t M,
+                              int64_t N, int64_t K, const float *sa,
+                              int64_t ld_sa, const float *sb, int64_t ld_sb,
+                              cudaStream_t s, int withhold) {
   if (M < 0 || N < 0 || K < 0) return FP8LA_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return FP8LA_OK;
   if (!C || ldc < N) return FP8LA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(C) & 1u) != 0) return FP8LA_ERR_ALIGNMENT;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (K == 0) {
     if (!device_is_sm10x()) return FP8LA_ERR_UNSUPPORTED;
     const int sms = sm_count();
@@ -488,6 +493,7 @@ extern "C" fp8la_status fp8_gemm_blockscaled_32x32(
   args.status = status;
   args.timeout_ns = wait_timeout_ns();
   args.c_vec16 = aligned16(C) && ldc % 8 == 0;
+  args.withhold_first = withhold;
   if (once_per_device(4, [] {
         return cudaFuncSetAttribute(gemm_e4m3_block32_kernel,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -501,4 +507,27 @@ extern "C" fp8la_status fp8_gemm_blockscaled_32x32(
   gemm_e4m3_block32_kernel<<<grid, kThreads, Lay::kAlloc, s>>>(tmA, tmB, tmSa,
                                                                tmSb, args);
   return launch_status();
+}
+
+}  // namespace
+
+fp8la_status diag_block32_withheld(const uint8_t *A, int64_t lda,
+                                   const uint8_t *B, int64_t ldb, uint16_t *C,
+                                   int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                   const float *sa, int64_t ld_sa,
+                                   const float *sb, int64_t ld_sb,
+                                   cudaStream_t s) {
+  if (M <= 0 || N <= 0 || K <= 0) return FP8LA_ERR_INVALID_ARG;
+  return blockscaled_impl(A, lda, B, ldb, C, ldc, M, N, K, sa, ld_sa, sb,
+                          ld_sb, s, 1);
+}
+
+}  // namespace fp8la
+
+extern "C" fp8la_status fp8_gemm_blockscaled_32x32(
+    const uint8_t *A, int64_t lda, const uint8_t *B, int64_t ldb, uint16_t *C,
+    int64_t ldc, int64_t M, int64_t N, int64_t K, const float *sa,
+    int64_t ld_sa, const float *sb, int64_t ld_sb, fp8la_stream_t stream) {
+  return blockscaled_impl(A, lda, B, ldb, C, ldc, M, N, K, sa, ld_sa, sb,
+                          ld_sb, reinterpret_cast<cudaStream_t>(stream), 0);
 }

@@ -46,6 +46,20 @@ cudaError_t once_per_device(int slot, F &&fn);
 int cached_clusters(int slot);
 void cache_clusters(int slot, int clusters);
 
+// Diagnostics (bounded-wait tests): the CTA-pair per-tensor GEMM and the
+// block-scaled GEMM with their first TMA arrival withheld.
+fp8la_status diag_pair_withheld(const uint8_t *A, int64_t lda, const uint8_t *B,
+                                int64_t ldb, uint16_t *C, int64_t ldc,
+                                int64_t M, int64_t N, int64_t K,
+                                const float *scale_a, const float *scale_b,
+                                cudaStream_t s);
+fp8la_status diag_block32_withheld(const uint8_t *A, int64_t lda,
+                                   const uint8_t *B, int64_t ldb, uint16_t *C,
+                                   int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                   const float *sa, int64_t ld_sa,
+                                   const float *sb, int64_t ld_sb,
+                                   cudaStream_t s);
+
 inline bool aligned16(const void *p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }

@@ -9,8 +9,10 @@
 
 namespace fp8la {
 
-// Bit set in the device status word when a bounded wait runs out.
+// Bits of the device status word: a bounded wait ran out; a kernel found a
+// device-side argument it cannot use (grouped GEMM m_offsets).
 constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusBadDeviceArg = 2u;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

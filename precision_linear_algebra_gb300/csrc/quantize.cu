@@ -543,6 +543,9 @@ fp8la_status quantize_pertensor_impl(const float *x, int64_t rows,
                                      float *scale_out, cudaStream_t s) {
   if (!amax_out || !scale_out || rows < 0 || cols < 0)
     return FP8LA_ERR_INVALID_ARG;
+  // The cast blocks read amax_out while the first of them writes scale_out.
+  if (static_cast<void *>(amax_out) == static_cast<void *>(scale_out))
+    return FP8LA_ERR_INVALID_ARG;
   const bool empty = rows == 0 || cols == 0;
   if (!empty && (!x || !q || ldx < cols || ldq < cols))
     return FP8LA_ERR_INVALID_ARG;

@@ -47,6 +47,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings_and_version(lib):
     assert lib.fp8la_status_string(0) == b"FP8LA_OK"
     assert lib.fp8la_status_string(-5) == b"FP8LA_ERR_DEVICE_TIMEOUT"
+    assert lib.fp8la_status_string(-6) == b"FP8LA_ERR_DEVICE_ARG"
     assert lib.fp8la_version() >= 100
 
 
@@ -58,6 +59,11 @@ def test_host_argument_rejection(lib):
     assert lib.fp8_quantize_pertensor(one, 4, 4, 4, one, 4, None, one, None) == -1
     assert lib.fp8_quantize_pertensor(one, -1, 4, 4, one, 4, one, one, None) == -1
     assert lib.fp8_quantize_pertensor(one, 4, 8, 4, one, 8, one, one, None) == -1
+    # amax_out and scale_out must be two different words
+    two = P(32)
+    assert lib.fp8_quantize_pertensor(one, 4, 4, 4, one, 4, two, two, None) == -1
+    assert lib.fp8_quantize_pertensor_ex(one, 4, 4, 4, one, 4, two, two, 0, None) == -1
+    assert lib.fp8_quantize_pertensor_ex(one, 0, 4, 4, one, 4, two, two, 1, None) == -1
     assert lib.fp8_quantize_blockwise_32x32(one, 4, 64, 64, one, 64, one, 1, None) == -1
     # delayed scaling: the carried-over amax, the new amax and the scale must
     # be three different words; bad format
@@ -116,7 +122,9 @@ def test_no_cpu_fallback_without_a_gpu(lib):
     assert torch.all(C == 7.0)
     x = torch.ones((4, 4))
     q = torch.zeros((4, 4), dtype=torch.uint8)
-    with pytest.raises(fl.Fp8laError):
+    s2 = torch.ones(1)
+    with pytest.raises(fl.Fp8laError) as e:
         fl.fp8_quantize_pertensor(x.data_ptr(), 4, 4, 4, q.data_ptr(), 4, s.data_ptr(),
-                                  s.data_ptr(), None)
+                                  s2.data_ptr(), None)
+    assert e.value.status in (-3, -4)
     assert torch.all(q == 0)

@@ -7,6 +7,7 @@ import os
 import numpy as np
 import pytest
 
+import _sweep
 import oracle
 from _helpers import bf16_to_f64, lib, to_dev
 from precision_linear_algebra_gb300 import workloads
@@ -65,13 +66,13 @@ def test_cast_sweep_e5m2_sampled():
         _sweep_chunk(bits, vec4=False)
 
 
-@pytest.mark.skipif(os.environ.get("FP8LA_EXHAUSTIVE") != "1",
-                    reason="set FP8LA_EXHAUSTIVE=1 for the full 2^32 sweep")
+@pytest.mark.skipif(os.environ.get("FP8LA_QUICK") == "1",
+                    reason="FP8LA_QUICK=1 leaves out the full 2^32 sweeps")
 def test_cast_sweep_e5m2_exhaustive():
-    """Every fp32 bit pattern through the 16-byte E5M2 quantiser path."""
-    for top in range(256):
-        lo = np.uint64(top) << np.uint64(24)
-        _sweep_chunk((np.arange(1 << 24, dtype=np.uint64) + lo).astype(np.uint32))
+    """Every fp32 bit pattern through the 16-byte E5M2 quantiser path, bit
+    for bit against the oracle (run in worker processes)."""
+    fl = lib()
+    _sweep.sweep_all("e5m2", lambda x: _quantize(fl, x))
 
 
 @pytest.fixture(params=[1, 2], ids=["single_cta", "cta_pair"])

@@ -128,3 +128,81 @@ def test_moe_layer_full_size_sampled(variant):
         rows = np.sort(rng.choice(hi - lo, min(48, hi - lo), replace=False))
         check_pertensor(Cn[lo + rows][:, cols], qx_n[lo:hi], qw_n[e], sx_n[e], sw_n[e],
                         rows=rows, cols=cols, what="expert %d" % e)
+
+
+def _launch_raw(fl, E, d_off, cap, dA, kp, dB, N, dC, ldc, K, d_sa, d_sb):
+    import torch
+    fl.fp8_grouped_gemm(E, d_off.data_ptr(), cap, dA.data_ptr(), kp, dB.data_ptr(), kp,
+                        N * kp, dC.data_ptr(), ldc, N, K, d_sa.data_ptr(), d_sb.data_ptr(),
+                        torch.cuda.current_stream().cuda_stream)
+
+
+@pytest.mark.parametrize("offsets", [
+    [0, 100, 200, 256 + 40],          # last offset past m_capacity (256)
+    [0, 120, 60, 200],                # a decreasing pair
+    [8, 100, 150, 200],               # does not start at 0
+    [0, 300, 280, 256],               # past capacity inside, back at the end
+], ids=["past_capacity", "decreasing", "nonzero_start", "overshoot_inside"])
+@pytest.mark.parametrize("K", [128, 0], ids=["K128", "K0"])
+def test_bad_offsets_write_nothing_and_are_reported(offsets, K, variant):
+    """m_offsets that break the contract are caught on the device: nothing is
+    written (C and guard rows past m_capacity, in the same allocation, keep
+    their sentinel), the status word says FP8LA_ERR_DEVICE_ARG, and a valid
+    call right after is correct."""
+    import torch
+    fl = lib()
+    rng = np.random.default_rng(77)
+    E, N, cap, guard = 3, 256, 256, 64
+    kp = 128
+    A = random_codes(rng, (cap + guard, kp))
+    B = random_codes(rng, (E, N, kp))
+    dA, dB = to_dev(A), to_dev(B)
+    dC = torch.full((cap + guard, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    d_sa = to_dev(np.full(E, 0.5, np.float32))
+    d_sb = to_dev(np.full(E, 0.25, np.float32))
+    stream = torch.cuda.current_stream().cuda_stream
+    assert fl.fp8_get_device_status(stream) == 0
+    _launch_raw(fl, E, to_dev(np.asarray(offsets, np.int32)), cap, dA, kp, dB, N, dC, N,
+                K, d_sa, d_sb)
+    assert fl.fp8_get_device_status(stream) == fl.FP8LA_ERR_DEVICE_ARG
+    assert fl.fp8_get_device_status(stream) == 0          # cleared by the read
+    assert torch.all(dC == 7.0), "a call with bad offsets wrote to C"
+    # the same buffers with valid offsets
+    good = np.array([0, 100, 100, 230], np.int32)
+    _launch_raw(fl, E, to_dev(good), cap, dA, kp, dB, N, dC, N, kp, d_sa, d_sb)
+    assert fl.fp8_get_device_status(stream) == 0
+    got = bf16_to_f64(dC)
+    for e in range(E):
+        lo, hi = good[e], good[e + 1]
+        if hi > lo:
+            check_pertensor(got[lo:hi], A[lo:hi], B[e], np.float32(0.5), np.float32(0.25),
+                            what="group %d after bad offsets" % e)
+    assert np.all(got[good[-1]:] == 7.0)
+
+
+def test_rows_past_the_last_group_are_ignored(variant):
+    """Rows of A past m_offsets[E] hold NaN codes (0x7F) and trailing groups
+    are empty: the valid rows match the oracle, no NaN leaks in, and C rows
+    past m_offsets[E] keep their sentinel."""
+    import torch
+    fl = lib()
+    rng = np.random.default_rng(78)
+    counts = [70, 0, 260, 3] + [0] * 12
+    E = len(counts)
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    N, K, cap = 320, 192, 700
+    A = np.full((cap, K), 0x7F, np.uint8)
+    A[:offs[-1]] = random_codes(rng, (int(offs[-1]), K))
+    B = random_codes(rng, (E, N, K))
+    dA, dB = to_dev(A), to_dev(B)
+    dC = torch.full((cap, N), -2.0, dtype=torch.bfloat16, device="cuda")
+    sa = rng.uniform(0.1, 2, E).astype(np.float32)
+    sb = rng.uniform(0.1, 2, E).astype(np.float32)
+    _launch_raw(fl, E, to_dev(offs), cap, dA, K, dB, N, dC, N, K, to_dev(sa), to_dev(sb))
+    assert fl.device_status() == 0
+    got = bf16_to_f64(dC)
+    for e in range(E):
+        lo, hi = offs[e], offs[e + 1]
+        if hi > lo:
+            check_pertensor(got[lo:hi], A[lo:hi], B[e], sa[e], sb[e], what="group %d" % e)
+    assert np.all(got[offs[-1]:] == -2.0)

@@ -5,6 +5,7 @@ import os
 import numpy as np
 import pytest
 
+import _sweep
 import oracle
 from _helpers import lib, to_dev
 from precision_linear_algebra_gb300 import workloads
@@ -122,15 +123,13 @@ def test_cast_sweep_sampled():
     _sweep_chunk(fl, rng.integers(0, 2 ** 32, size=1 << 24, dtype=np.uint64).astype(np.uint32))
 
 
-@pytest.mark.skipif(os.environ.get("FP8LA_EXHAUSTIVE") != "1",
-                    reason="set FP8LA_EXHAUSTIVE=1 for the full 2^32 sweep")
+@pytest.mark.skipif(os.environ.get("FP8LA_QUICK") == "1",
+                    reason="FP8LA_QUICK=1 leaves out the full 2^32 sweeps")
 def test_cast_sweep_exhaustive():
     """Every fp32 bit pattern through the 16-byte quantiser path, 2^24 at a
-    time (about ten minutes, most of it the oracle)."""
+    time, bit for bit against the oracle (run in worker processes)."""
     fl = lib()
-    for top in range(256):
-        lo = np.uint64(top) << np.uint64(24)
-        _sweep_chunk(fl, (np.arange(1 << 24, dtype=np.uint64) + lo).astype(np.uint32))
+    _sweep.sweep_all("e4m3", lambda x: _run_pertensor(fl, x))
 
 
 @pytest.mark.parametrize("shape,pad", [((64, 64), 0), ((70, 100), 0), ((33, 31), 5),
