@@ -639,7 +639,9 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     }
   } else if (warp == 5) {
     // ------------------------------------------------- MMA (leader CTA only)
-    if (lane == 0 && leader) {
+    // The whole warp runs the loop and waits; one elected lane issues each
+    // MMA and commit, so the warp never branches around them.
+    if (leader) {
       const uint32_t idesc_whole = idesc_e4m3_f32(P_BM, P_BN) | a.fmt_bits;
       const uint32_t idesc_half = idesc_e4m3_f32(P_BM, P_BN / 2) | a.fmt_bits;
       uint32_t s = 0, ph = 0, local = 0;
@@ -647,16 +649,18 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       for (int i = cluster_id; ok && i < n_items; i += num_clusters, ++local) {
         const uint32_t idesc = i < n_whole ? idesc_whole : idesc_half;
         const uint32_t buf = local & 1u, use = local >> 1;
-        if (!mbar_wait(tempty_bar(buf), (use & 1u) ^ 1u, a.timeout_ns,
-                       a.status, abort_flag)) {
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(tempty_bar(buf), (use & 1u) ^ 1u,
+                                  a.timeout_ns, a.status, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * P_BN;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(full_bar(s), ph, a.timeout_ns, a.status,
-                         abort_flag)) {
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait(full_bar(s), ph, a.timeout_ns, a.status,
+                                    abort_flag))) {
             ok = false;
             break;
           }
@@ -667,15 +671,15 @@ __global__ void __launch_bounds__(P_THREADS, 1)
               smem_desc_k128_sw128(base + L::kB + s * L::kBBytes);
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k)
-            umma_f8f6f4_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc,
-                             (kb | k) != 0 ? 1u : 0u);
-          umma_commit_pair(empty_bar(s), 0x3);
+            umma_f8f6f4_pair_warp(d_tmem, adesc + 2u * k, bdesc + 2u * k,
+                                  idesc, (kb | k) != 0 ? 1u : 0u);
+          umma_commit_pair_warp(empty_bar(s), 0x3);
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
-        umma_commit_pair(tfull_bar(buf), 0x3);
+        umma_commit_pair_warp(tfull_bar(buf), 0x3);
       }
-      umma_commit_pair(final_bar, 0x1);
+      umma_commit_pair_warp(final_bar, 0x1);
       mbar_wait_drain(final_bar, 0, a.timeout_ns, a.status);
     }
   } else {

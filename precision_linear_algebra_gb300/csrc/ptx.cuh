@@ -380,6 +380,36 @@ __device__ __forceinline__ void umma_f8f6f4_pair(uint32_t d_tmem,
       : "memory");
 }
 
+// As umma_f8f6f4_pair, executed by a whole converged warp: one elected lane
+// issues the MMA (the warp does not branch around it).
+__device__ __forceinline__ void umma_f8f6f4_pair_warp(uint32_t d_tmem,
+                                                      uint64_t adesc,
+                                                      uint64_t bdesc,
+                                                      uint32_t idesc,
+                                                      uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// As umma_commit_pair, executed by a whole converged warp (one elected lane
+// commits).
+__device__ __forceinline__ void umma_commit_pair_warp(uint32_t bar,
+                                                      uint16_t cta_mask) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster."
+      "multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
 // Arrive once on the barrier at CTA-relative address `bar` in every CTA of
 // `cta_mask` when this thread's earlier tcgen05 operations have completed.
 __device__ __forceinline__ void umma_commit_pair(uint32_t bar,
