@@ -130,7 +130,9 @@ def test_k_zero_writes_zeros():
 def test_transformer_linears_full_size_sampled(name):
     """M=4096 tokens through each 70B-class linear: 32x32 block quantisation
     of activations and weights on the GPU (checked against the oracle on
-    sampled tiles), then the block-scaled GEMM checked on sampled outputs."""
+    sampled tiles), then the block-scaled GEMM checked on sampled outputs,
+    on one whole 128-row tile row of C and on one whole 64-column tile
+    column."""
     import torch
     fl = lib()
     X, W = workloads.transformer_linear(name, seed=0)
@@ -149,9 +151,24 @@ def test_transformer_linears_full_size_sampled(name):
         rq, rs = oracle.quantize_blockwise_32x32(src[r0:r0 + 64, c0:c0 + 64])
         assert np.array_equal(q[r0:r0 + 64, c0:c0 + 64], rq)
         assert np.array_equal(s[r0 // 32:r0 // 32 + 2, c0 // 32:c0 // 32 + 2], rs)
+    maxes = (oracle.max_abs_tile_scaled_32x32(A, sa), oracle.max_abs_tile_scaled_32x32(B, sb))
     rows = np.sort(rng.choice(A.shape[0], 64, replace=False))
     cols = np.sort(rng.choice(B.shape[0], 64, replace=False))
     Cn = bf16_to_f64(C[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()])
-    check_block(Cn, A, B, sa, sb, rows=rows, cols=cols, what=name,
-                maxes=(oracle.max_abs_tile_scaled_32x32(A, sa),
-                                   oracle.max_abs_tile_scaled_32x32(B, sb)))
+    check_block(Cn, A, B, sa, sb, rows=rows, cols=cols, what=name, maxes=maxes)
+    # one whole 128-row tile row of C (every column tile, every K block) and
+    # one whole 64-column tile column (every row tile), in bounded chunks
+    M, N = C.shape
+    r0 = int(rng.integers(0, M // 128)) * 128
+    c0 = int(rng.integers(0, N // 64)) * 64
+    Cg = C[r0:r0 + 128].float().cpu().numpy().astype(np.float64)
+    step = max(512, (1 << 25) // A.shape[1])     # decoded B chunk <= 256 MB
+    for j0 in range(0, N, step):
+        cols = np.arange(j0, min(N, j0 + step))
+        check_block(Cg[:, j0:j0 + cols.size], A, B, sa, sb, rows=np.arange(r0, r0 + 128),
+                    cols=cols, what="%s rows %d.." % (name, r0), maxes=maxes)
+    Cg = C[:, c0:c0 + 64].float().cpu().numpy().astype(np.float64)
+    for i0 in range(0, M, 1024):
+        rows = np.arange(i0, min(M, i0 + 1024))
+        check_block(Cg[i0:i0 + rows.size], A, B, sa, sb, rows=rows,
+                    cols=np.arange(c0, c0 + 64), what="%s cols %d.." % (name, c0), maxes=maxes)
