@@ -114,6 +114,8 @@ struct TileInfo {
   int32_t row_end;  // rows >= row_end are not stored
   int32_t n0;
   int32_t group;
+  int32_t tn;       // CTA-pair grouped tail tile computed transposed: its
+                    // MMA width (a multiple of 32, <= 256); 0 otherwise
 };
 
 template <bool GROUPED, int TBM>
@@ -122,6 +124,7 @@ __device__ __forceinline__ TileInfo tile_info(int t, const GemmArgs &a,
                                               const int32_t *offs_smem,
                                               int BN) {
   TileInfo ti;
+  ti.tn = 0;
   if (!GROUPED) {
     const int tiles_m = (a.M + TBM - 1) / TBM;
     int mb, nb;
@@ -147,6 +150,12 @@ __device__ __forceinline__ TileInfo tile_info(int t, const GemmArgs &a,
     ti.row_end = min(m_hi, a.M);   // m_offsets are checked at set-up as well
     ti.n0 = nb * BN;
     ti.group = e;
+    // A group's last row tile, when partial, is computed transposed by the
+    // CTA-pair kernel (C_tail^T = B_e A_tail^T: MMA M = 256 over C columns,
+    // N = the tail's rows rounded up to 32) instead of as a 256-row tile
+    // whose rows past the group are padding.
+    const int rows = ti.row_end - ti.row0;
+    if (TBM == 256 && rows < TBM) ti.tn = (rows + 31) & ~31;
   }
   return ti;
 }
@@ -210,6 +219,26 @@ __device__ __forceinline__ void store_chunk32(uint32_t taddr, bool row_ok,
         crow[n + j] = static_cast<uint16_t>((j & 1) ? (w[j >> 1] >> 16)
                                                     : (w[j >> 1] & 0xFFFFu));
   }
+}
+
+// Epilogue of a transposed tile: this lane's TMEM row is C column n, its 32
+// TMEM columns from taddr are C rows m0 .. m0+31; rows at or past m_end and
+// columns at or past N are not stored.  Across the warp each store writes 32
+// consecutive BF16 of one C row.  Every lane of the warp must call it.
+__device__ __forceinline__ void store_chunk32_t(uint32_t taddr, uint16_t *C,
+                                                int64_t ldc, int m0, int m_end,
+                                                int n, int N, float scale) {
+  uint32_t v[32];
+  tmem_ld32(taddr, v);
+  if (n >= N) return;
+  uint16_t *cp = C + static_cast<int64_t>(m0) * ldc + n;
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    if (m0 + j < m_end) {
+      const __nv_bfloat16 h =
+          __float2bfloat16_rn(__fmul_rn(__uint_as_float(v[j]), scale));
+      cp[static_cast<int64_t>(j) * ldc] = *reinterpret_cast<const uint16_t *>(&h);
+    }
 }
 
 // As store_chunk32, for a whole 32 x 32 block through a TMA store: the warp
@@ -598,9 +627,13 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       for (int i = cluster_id; ok && i < n_items; i += num_clusters) {
         int half;
         const TileInfo ti = item(i, half);
-        // A whole tile takes 128 B rows per CTA, a half tile 64.
+        // A whole tile takes 128 B rows per CTA, a half tile 64.  A
+        // transposed tail tile puts this CTA's 128 rows of B_e in the A
+        // slot (the MMA's M operand) and the tail rows of A, tn / 2 per CTA
+        // (a 128-row box, of which the MMA reads the first tn / 2 <= 128),
+        // in the B slot.
         const int brows = half < 0 ? 128 : 64;
-        const int arow = ti.row0 + 128 * static_cast<int>(rank);
+        const int arow = ti.row0 + (ti.tn ? ti.tn / 2 : 128) * static_cast<int>(rank);
         const int brow = ti.n0 + brows * static_cast<int>(rank);
         const uint32_t bytes = 2u * (L::kABytes + brows * BK);
         for (int kb = 0; kb < nkb; ++kb) {
@@ -614,11 +647,13 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           // (Diagnostic only: the second CTA leaves out its first loads, so
           // the leader's first stage never fills.)
           if (!(a.withhold_first && !leader && issued == 0)) {
-            tma_load_2d_pair(base + L::kA + s * L::kABytes, &tmA, lf, kb * BK,
-                             arow);
+            const uint32_t aslot = base + (ti.tn ? L::kB + s * L::kBBytes
+                                                 : L::kA + s * L::kABytes);
+            const uint32_t bslot = base + (ti.tn ? L::kA + s * L::kABytes
+                                                 : L::kB + s * L::kBBytes);
+            tma_load_2d_pair(aslot, &tmA, lf, kb * BK, arow);
             if (GROUPED)
-              tma_load_3d_pair(base + L::kB + s * L::kBBytes, &tmB, lf,
-                               kb * BK, brow, ti.group);
+              tma_load_3d_pair(bslot, &tmB, lf, kb * BK, brow, ti.group);
             else
               tma_load_2d_pair(base + L::kB + s * L::kBBytes,
                                half < 0 ? &tmB : &tmB64, lf, kb * BK, brow);
@@ -647,7 +682,12 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       uint32_t s = 0, ph = 0, local = 0;
       bool ok = true;
       for (int i = cluster_id; ok && i < n_items; i += num_clusters, ++local) {
-        const uint32_t idesc = i < n_whole ? idesc_whole : idesc_half;
+        uint32_t idesc = i < n_whole ? idesc_whole : idesc_half;
+        if (GROUPED) {
+          int half;
+          const TileInfo ti = item(i, half);
+          if (ti.tn) idesc = idesc_e4m3_f32(P_BM, ti.tn) | a.fmt_bits;
+        }
         const uint32_t buf = local & 1u, use = local >> 1;
         if (!__all_sync(0xffffffffu,
                         mbar_wait(tempty_bar(buf), (use & 1u) ^ 1u,
@@ -708,6 +748,27 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                                    a.status, abort_flag);
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after();
+      if (GROUPED && ti.tn) {
+        // Transposed tail tile: TMEM lane = C column, TMEM column = C row;
+        // the two warps of a lane quarter take alternate 32-row chunks.
+        const int n = ti.n0 + 128 * static_cast<int>(rank) + quarter * 32 + lane;
+        const uint32_t tbase = tmem_base +
+                               (static_cast<uint32_t>(quarter * 32) << 16) +
+                               buf * P_BN;
+#pragma unroll 1
+        for (int c = 32 * col_half; c < ti.tn; c += 64)
+          store_chunk32_t(tbase + c, a.C, a.ldc, ti.row0 + c, ti.row_end, n, a.N,
+                          scale);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader)
+            mbar_arrive(tempty_bar(buf));
+          else
+            mbar_arrive_cluster(buf ? leader_tempty1 : leader_tempty0);
+        }
+        continue;
+      }
       const int row_chunk0 =
           ti.row0 + 128 * static_cast<int>(rank) + quarter * 32;
       const int row = row_chunk0 + lane;

@@ -206,3 +206,26 @@ def test_rows_past_the_last_group_are_ignored(variant):
         if hi > lo:
             check_pertensor(got[lo:hi], A[lo:hi], B[e], sa[e], sb[e], what="group %d" % e)
     assert np.all(got[offs[-1]:] == -2.0)
+
+
+@pytest.mark.parametrize("N,K", [(300, 192), (512, 128)])
+def test_tail_tiles_of_every_size(N, K, variant):
+    """Groups whose last row tile holds 1..255 rows (the CTA-pair kernel
+    computes tails of at most 128 rows transposed), N not a multiple of the
+    tile width; every group against the oracle, rows past the last group
+    untouched."""
+    fl = lib()
+    rng = np.random.default_rng(N + K)
+    counts = [1, 16, 31, 32, 33, 64, 96, 100, 127, 128, 129, 255, 256, 257, 300, 0, 513]
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    E = len(counts)
+    A = random_codes(rng, (int(offs[-1]), K))
+    B = random_codes(rng, (E, N, K))
+    sa = rng.uniform(0.01, 2, E).astype(np.float32)
+    sb = rng.uniform(0.01, 2, E).astype(np.float32)
+    got = _grouped(fl, A, offs, B, sa, sb, cap_extra=45)
+    for e in range(E):
+        lo, hi = offs[e], offs[e + 1]
+        if hi > lo:
+            check_pertensor(got[lo:hi], A[lo:hi], B[e], sa[e], sb[e], what="group %d" % e)
+    assert np.all(got[offs[-1]:] == 3.0), "rows past the last group were written"
