@@ -314,7 +314,9 @@ FP8LA_API fp8la_status fp8la_diag_withheld_arrival(
  * afterwards from this process: 0 = by problem shape (default), 1 = the
  * single-CTA kernel (128 x 256 tiles), 2 = the CTA-pair kernel (256 x 256
  * tiles on two SMs, tcgen05 cta_group::2), 3 = the single-CTA kernel with
- * 128 x 128 tiles (fp8_gemm only; fp8_grouped_gemm treats 3 as 0).  All
+ * 128 x 128 tiles, 4 = two CTA pairs per cluster of four sharing the rows
+ * of A by TMA multicast (3 and 4: fp8_gemm only; fp8_grouped_gemm treats
+ * them as 0).  All
  * compute the same result within the documented bound; this exists for
  * testing and tuning.  Other values return FP8LA_ERR_INVALID_ARG.
  */

@@ -166,7 +166,8 @@ def fp8la_diag_withheld_arrival(kernel, A, lda, B, ldb, C, ldc, M, N, K, scale_a
 
 
 def fp8la_set_gemm_variant(variant):
-    """0 = by shape, 1 = single-CTA kernel, 2 = CTA-pair kernel."""
+    """0 = by shape, 1 = single-CTA kernel, 2 = CTA-pair kernel, 3 = single-CTA
+    kernel with 128 x 128 tiles, 4 = two CTA pairs per cluster sharing A."""
     return _call("fp8la_set_gemm_variant", int(variant))
 
 

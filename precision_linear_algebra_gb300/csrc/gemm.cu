@@ -526,13 +526,23 @@ static_assert(PairSmem::kB % 1024 == 0 && PairSmem::kABytes % 1024 == 0 &&
               "pair layout");
 static_assert(PairSmem::kAlloc <= 227 * 1024, "shared memory");
 
-template <bool GROUPED>
+// QUAD (per-tensor GEMM only): clusters of four CTAs, two CTA pairs that
+// compute horizontally adjacent 256 x 256 tiles (one 256 x 512 cluster tile)
+// and so need the same rows of A.  Each CTA loads 64 of the 128 A rows its
+// pair position needs and multicasts them to itself and to the CTA at the
+// same position in the other pair, which loads the other 64: every A byte
+// leaves L2 once per cluster instead of once per pair.  A stage is refilled
+// only after both pairs' MMAs have finished with it (each pair's commit
+// arrives on the stage's empty barrier in all four CTAs).
+template <bool GROUPED, bool QUAD = false>
 __global__ void __launch_bounds__(P_THREADS, 1)
     gemm_e4m3_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmB64,
                           const __grid_constant__ CUtensorMap tmC,
+                          const __grid_constant__ CUtensorMap tmA64,
                           const GemmArgs a) {
+  static_assert(!(GROUPED && QUAD), "clusters of four: per-tensor GEMM only");
   using L = PairSmem;
   constexpr int STAGES = P_STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -547,7 +557,10 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   // stream serialization).
   if (GROUPED) pdl_wait();
   const uint32_t rank = cluster_ctarank();
-  const bool leader = rank == 0;
+  const uint32_t pair = QUAD ? rank >> 1 : 0;      // which CTA pair
+  const uint32_t prank = rank & 1u;                // position in the pair
+  const uint32_t lrank = rank & ~1u;               // this pair's leader
+  const bool leader = prank == 0;
 
   const uint32_t bar0 = base + L::kBar;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -561,15 +574,17 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   int32_t *pref = reinterpret_cast<int32_t *>(sbase + L::kPrefix);
   __shared__ int32_t offs_smem[GROUPED ? kMaxGroups + 1 : 1];
 
-  const int tiles_n = (a.N + P_BN - 1) / P_BN;
+  // Column tiles of the work items: 256 per pair, 512 per cluster of four.
+  constexpr int kCBN = QUAD ? 2 * P_BN : P_BN;
+  const int tiles_n = (a.N + kCBN - 1) / kCBN;
   const int nkb = (a.K + BK - 1) / BK;
-  const int cluster_id = blockIdx.x >> 1;
-  const int num_clusters = gridDim.x >> 1;
+  const int cluster_id = QUAD ? blockIdx.x >> 2 : blockIdx.x >> 1;
+  const int num_clusters = QUAD ? gridDim.x >> 2 : gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), QUAD ? 2 : 1);   // one commit per pair
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -580,7 +595,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     fence_mbar_init();
   }
   if (warp == 4 && lane == 0) {
-    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(QUAD ? &tmA64 : &tmA);
     tma_prefetch_desc(&tmB);
     if (a.split_tail > 0) tma_prefetch_desc(&tmB64);
   }
@@ -614,8 +629,14 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       t = n_whole + ((i - n_whole) >> 1);
       half = (i - n_whole) & 1;
     }
-    TileInfo ti = tile_info<GROUPED, P_BM>(t, a, tiles_n, pref, offs_smem, P_BN);
-    if (half >= 0) ti.n0 += 128 * half;
+    TileInfo ti = tile_info<GROUPED, P_BM>(t, a, tiles_n, pref, offs_smem, kCBN);
+    // A cluster of four splits its 512 columns between the pairs: 256 each
+    // for a whole tile, 128 each for a half (half h covers 256 h .. +255).
+    if (QUAD)
+      ti.n0 += half < 0 ? 256 * static_cast<int>(pair)
+                        : 256 * half + 128 * static_cast<int>(pair);
+    else if (half >= 0)
+      ti.n0 += 128 * half;
     return ti;
   };
 
@@ -633,8 +654,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         // (a 128-row box, of which the MMA reads the first tn / 2 <= 128),
         // in the B slot.
         const int brows = half < 0 ? 128 : 64;
-        const int arow = ti.row0 + (ti.tn ? ti.tn / 2 : 128) * static_cast<int>(rank);
-        const int brow = ti.n0 + brows * static_cast<int>(rank);
+        const int arow = ti.row0 + (ti.tn ? ti.tn / 2 : 128) * static_cast<int>(prank);
+        const int brow = ti.n0 + brows * static_cast<int>(prank);
         const uint32_t bytes = 2u * (L::kABytes + brows * BK);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns, a.status,
@@ -642,7 +663,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             ok = false;
             break;
           }
-          const uint32_t lf = mapa_shared(full_bar(s), 0);
+          const uint32_t lf = mapa_shared(full_bar(s), lrank);
           if (leader) mbar_arrive_expect_tx(full_bar(s), bytes);
           // (Diagnostic only: the second CTA leaves out its first loads, so
           // the leader's first stage never fills.)
@@ -651,7 +672,15 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                                                  : L::kA + s * L::kABytes);
             const uint32_t bslot = base + (ti.tn ? L::kA + s * L::kABytes
                                                  : L::kB + s * L::kBBytes);
-            tma_load_2d_pair(aslot, &tmA, lf, kb * BK, arow);
+            if (QUAD)
+              // This CTA's 64-row half of its A rows, to itself and to the
+              // CTA at the same position in the other pair.
+              tma_load_2d_pair_mc(aslot + 8192u * pair, &tmA64, lf, kb * BK,
+                                  arow + 64 * static_cast<int>(pair),
+                                  static_cast<uint16_t>((1u << rank) |
+                                                        (1u << (rank ^ 2u))));
+            else
+              tma_load_2d_pair(aslot, &tmA, lf, kb * BK, arow);
             if (GROUPED)
               tma_load_3d_pair(bslot, &tmB, lf, kb * BK, brow, ti.group);
             else
@@ -713,13 +742,14 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           for (int k = 0; k < BK / UMMA_K; ++k)
             umma_f8f6f4_pair_warp(d_tmem, adesc + 2u * k, bdesc + 2u * k,
                                   idesc, (kb | k) != 0 ? 1u : 0u);
-          umma_commit_pair_warp(empty_bar(s), 0x3);
+          umma_commit_pair_warp(empty_bar(s), QUAD ? 0xF : 0x3);
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
-        umma_commit_pair_warp(tfull_bar(buf), 0x3);
+        umma_commit_pair_warp(tfull_bar(buf),
+                              static_cast<uint16_t>(0x3u << (2u * pair)));
       }
-      umma_commit_pair_warp(final_bar, 0x1);
+      umma_commit_pair_warp(final_bar, static_cast<uint16_t>(1u << rank));
       mbar_wait_drain(final_bar, 0, a.timeout_ns, a.status);
     }
   } else {
@@ -727,8 +757,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     uint32_t local = 0;
     float scale = 1.0f;
     int cur_group = -1;
-    const uint32_t leader_tempty0 = mapa_shared(tempty_bar(0), 0);
-    const uint32_t leader_tempty1 = mapa_shared(tempty_bar(1), 0);
+    const uint32_t leader_tempty0 = mapa_shared(tempty_bar(0), lrank);
+    const uint32_t leader_tempty1 = mapa_shared(tempty_bar(1), lrank);
     const int quarter = warp & 3;                 // TMEM lanes 32*quarter..
     const int col_half = warp >= 6 ? 1 : 0;       // which half of the columns
     const uint32_t cstage = base + L::kCStage +
@@ -751,7 +781,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       if (GROUPED && ti.tn) {
         // Transposed tail tile: TMEM lane = C column, TMEM column = C row;
         // the two warps of a lane quarter take alternate 32-row chunks.
-        const int n = ti.n0 + 128 * static_cast<int>(rank) + quarter * 32 + lane;
+        const int n = ti.n0 + 128 * static_cast<int>(prank) + quarter * 32 + lane;
         const uint32_t tbase = tmem_base +
                                (static_cast<uint32_t>(quarter * 32) << 16) +
                                buf * P_BN;
@@ -770,7 +800,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         continue;
       }
       const int row_chunk0 =
-          ti.row0 + 128 * static_cast<int>(rank) + quarter * 32;
+          ti.row0 + 128 * static_cast<int>(prank) + quarter * 32;
       const int row = row_chunk0 + lane;
       const bool row_ok = row < ti.row_end;
       uint16_t *crow = a.C + static_cast<int64_t>(row) * a.ldc;
@@ -944,16 +974,18 @@ bool encode_c(CUtensorMap *m, const uint16_t *C, int64_t ldc, int64_t rows,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Launch the CTA-pair kernel on clusters of two CTAs, as many clusters as
-// can be resident at once (at most one per pair tile).
-template <bool GROUPED>
+// Launch the CTA-pair kernel on clusters of two CTAs (QUAD: four, two
+// pairs), as many clusters as can be resident at once (at most one per work
+// tile: a pair tile, or for QUAD a 256 x 512 cluster tile).
+template <bool GROUPED, bool QUAD = false>
 fp8la_status launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB,
                               const CUtensorMap &tmB64, const CUtensorMap &tmC,
-                              GemmArgs args, int64_t max_tiles,
-                              cudaStream_t s) {
+                              const CUtensorMap &tmA64, GemmArgs args,
+                              int64_t max_tiles, cudaStream_t s) {
   using L = PairSmem;
-  auto kern = gemm_e4m3_pair_kernel<GROUPED>;
-  const int slot = GROUPED ? 3 : 2;
+  auto kern = gemm_e4m3_pair_kernel<GROUPED, QUAD>;
+  constexpr int kCluster = QUAD ? 4 : 2;
+  const int slot = QUAD ? 6 : (GROUPED ? 3 : 2);
   if (once_per_device(slot, [&] {
         return cudaFuncSetAttribute(
             kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
@@ -962,7 +994,7 @@ fp8la_status launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB,
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = kCluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(P_THREADS, 1, 1);
@@ -970,7 +1002,7 @@ fp8la_status launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB,
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cfg.gridDim = dim3(2, 1, 1);
+  cfg.gridDim = dim3(kCluster, 1, 1);
   int clusters = cached_clusters(slot);
   if (clusters < 1) {
     if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess ||
@@ -988,7 +1020,7 @@ fp8la_status launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB,
   const int64_t items = max_tiles + args.split_tail;
   int64_t n = items < clusters ? items : clusters;
   if (n < 1) n = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * n), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(kCluster * n), 1, 1);
   // Plain GEMMs start while the previous kernel in the stream finishes (the
   // kernel waits for it before reading operands; see pdl_wait).
   cudaLaunchAttribute attrs[2] = {attr[0], {}};
@@ -996,14 +1028,15 @@ fp8la_status launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB,
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = GROUPED ? 1 : 2;
-  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmB64, tmC, args) !=
+  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmB64, tmC, tmA64, args) !=
       cudaSuccess)
     return FP8LA_ERR_CUDA;
   return launch_status();
 }
 
 // Kernel choice: 0 = by shape, 1 = single-CTA kernel (128 x 256 tiles),
-// 2 = CTA-pair kernel, 3 = single-CTA kernel with 128 x 128 tiles.
+// 2 = CTA-pair kernel, 3 = single-CTA kernel with 128 x 128 tiles, 4 = two
+// CTA pairs per cluster sharing A by multicast.
 std::atomic<int> g_variant{0};
 
 fp8la_status check_operands(const uint8_t *A, int64_t lda, const uint8_t *B,
@@ -1050,12 +1083,14 @@ fp8la_status gemm_pertensor_impl(const uint8_t *A, int64_t lda,
   const int64_t pair_tiles = ((M + P_BM - 1) / P_BM) * ((N + P_BN - 1) / P_BN);
   const bool small = !withhold &&
                      (v == 3 || (v == 0 && sms > 0 && pair_tiles * 4 < sms));
-  const bool pair = withhold == 2 ||
+  const bool quad = !withhold && !small && v == 4;
+  const bool pair = withhold == 2 || quad ||
                     (!withhold && !small && (v == 2 || (v == 0 && M > BM)));
-  CUtensorMap tmA, tmB, tmB64;
+  CUtensorMap tmA, tmB, tmB64, tmA64{};
   if (!encode_2d(&tmA, A, K, M, lda, BK, BM) ||
       !encode_2d(&tmB, B, K, N, ldb, BK, pair || small ? 128 : kBN) ||
-      (pair && !encode_2d(&tmB64, B, K, N, ldb, BK, 64)))
+      (pair && !encode_2d(&tmB64, B, K, N, ldb, BK, 64)) ||
+      (quad && !encode_2d(&tmA64, A, K, M, lda, BK, 64)))
     return FP8LA_ERR_CUDA;
   unsigned *status = status_word_ptr();
   if (!status) return FP8LA_ERR_CUDA;
@@ -1078,8 +1113,13 @@ fp8la_status gemm_pertensor_impl(const uint8_t *A, int64_t lda,
       if (!encode_c(&tmC, C, ldc, M, N)) return FP8LA_ERR_CUDA;
       args.c_tma = 1;
     }
+    if (quad) {
+      const int64_t ctiles = ((M + P_BM - 1) / P_BM) * ((N + 2 * P_BN - 1) / (2 * P_BN));
+      return launch_gemm_pair<false, true>(tmA, tmB, tmB64, tmC, tmA64, args,
+                                           ctiles, s);
+    }
     const int64_t tiles = ((M + P_BM - 1) / P_BM) * ((N + P_BN - 1) / P_BN);
-    return launch_gemm_pair<false>(tmA, tmB, tmB64, tmC, args, tiles, s);
+    return launch_gemm_pair<false>(tmA, tmB, tmB64, tmC, tmA64, args, tiles, s);
   }
   if (small) {
     const int64_t tiles = ((M + BM - 1) / BM) * ((N + kSmallBN - 1) / kSmallBN);
@@ -1171,7 +1211,7 @@ extern "C" fp8la_status fp8_grouped_gemm(
     return b_group_stride % 16 != 0 ? FP8LA_ERR_ALIGNMENT
                                     : FP8LA_ERR_INVALID_ARG;
   // CTA pairs when groups average at least one pair tile of rows.
-  const int v = g_variant.load() == 3 ? 0 : g_variant.load();
+  const int v = g_variant.load() >= 3 ? 0 : g_variant.load();
   const bool pair = v == 2 || (v == 0 && m_capacity >= int64_t(P_BM) * num_groups);
   CUtensorMap tmA, tmB;
   if (!encode_2d(&tmA, A, K, m_capacity, lda, BK, BM) ||
@@ -1203,7 +1243,7 @@ extern "C" fp8la_status fp8_grouped_gemm(
     }
     const int64_t tiles = ((m_capacity + P_BM - 1) / P_BM + num_groups) *
                           ((N + P_BN - 1) / P_BN);
-    return launch_gemm_pair<true>(tmA, tmB, tmB, tmC, args, tiles, s);
+    return launch_gemm_pair<true>(tmA, tmB, tmB, tmC, tmA, args, tiles, s);
   }
   const int64_t tiles =
       ((m_capacity + BM - 1) / BM + num_groups) * ((N + kBN - 1) / kBN);
@@ -1211,7 +1251,7 @@ extern "C" fp8la_status fp8_grouped_gemm(
 }
 
 extern "C" fp8la_status fp8la_set_gemm_variant(int32_t variant) {
-  if (variant < 0 || variant > 3) return FP8LA_ERR_INVALID_ARG;
+  if (variant < 0 || variant > 4) return FP8LA_ERR_INVALID_ARG;
   g_variant.store(variant);
   return FP8LA_OK;
 }

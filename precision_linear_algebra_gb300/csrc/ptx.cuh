@@ -329,6 +329,24 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap,
       : "memory");
 }
 
+// As tma_load_2d_pair, multicast: the box lands at CTA-relative address dst
+// in every CTA of cta_mask, and each destination's bytes are signalled on
+// the barrier at mbar's CTA-relative offset in that destination's pair
+// leader (mbar is given as the address in this CTA's own pair leader).
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst,
+                                                    const void *tmap,
+                                                    uint32_t mbar, int32_t c0,
+                                                    int32_t c1,
+                                                    uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::"
+      "complete_tx::bytes.multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(mbar), "r"(c0), "r"(c1),
+      "h"(cta_mask)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void *tmap,
                                                  uint32_t mbar, int32_t c0,
                                                  int32_t c1, int32_t c2) {

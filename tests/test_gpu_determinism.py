@@ -44,7 +44,7 @@ def _repeat(torch, fl, run, n=3):
     assert torch.equal(out, first)
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2])
+@pytest.mark.parametrize("variant", [0, 1, 2, 4])
 def test_pertensor_8192(variant):
     import torch
     fl = lib()

@@ -75,7 +75,7 @@ def test_cast_sweep_e5m2_exhaustive():
     _sweep.sweep_all("e5m2", lambda x: _quantize(fl, x))
 
 
-@pytest.fixture(params=[1, 2], ids=["single_cta", "cta_pair"])
+@pytest.fixture(params=[1, 2, 4], ids=["single_cta", "cta_pair", "cta_quad"])
 def variant(request):
     fl = lib()
     fl.fp8la_set_gemm_variant(request.param)

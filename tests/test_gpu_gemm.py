@@ -15,10 +15,11 @@ from precision_linear_algebra_gb300 import workloads
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=[1, 2, 3], ids=["single_cta", "cta_pair", "single_cta_128"])
+@pytest.fixture(params=[1, 2, 3, 4], ids=["single_cta", "cta_pair", "single_cta_128", "cta_quad"])
 def variant(request):
     """Run a test once per GEMM kernel (single-CTA 128 x 256 tiles, CTA
-    pair, single-CTA 128 x 128 tiles)."""
+    pair, single-CTA 128 x 128 tiles, two CTA pairs per cluster sharing A
+    by multicast)."""
     fl = lib()
     fl.fp8la_set_gemm_variant(request.param)
     yield request.param
