@@ -15,33 +15,44 @@
 // by one tcgen05.mma (M=128, N=64, K=32) into a fresh TMEM buffer and then
 // weighted and added on the CUDA cores.
 //
-// Design (one CTA per SM, persistent, 10 warps).  The promotion costs one
+// Design (one CTA per SM, persistent, 18 warps).  The promotion costs one
 // FP32 FMA per output per 32-wide K block, against 32 tensor-core FMAs: on
 // 128 FP32 lanes per SM versus 8192 tensor FMAs per clock this caps the
-// kernel near half the dense FP8 peak, so the design keeps the FMA pipe
-// busy and puts all synchronisation at the granularity of 128-wide K stages:
-//   * warp 8: producer (lane 0).  Per 128-wide K stage (8-stage ring) it
-//     issues four TMA loads on one barrier: a 128 x 128 A tile, a 64 x 128 B
-//     tile, and the stage's scale boxes sa[4 row tiles][4 K blocks] and
-//     sb[2 column tiles][4 K blocks].  Nothing on the producer waits for
-//     global memory, so it runs up to eight stages ahead.
-//   * warp 9: MMA issuer (lane 0).  Per stage, four MMAs (M=128, N=64, K=32,
+// kernel near half the dense FP8 peak.  What holds it below that is the
+// latency of each handoff between the MMA warp and the promotion warps, so
+// the CTA works on two output tiles at once and gives each its own
+// promotion group, which hides one group's waits behind the other's FMAs;
+// all synchronisation is at the granularity of 128-wide K stages:
+//   * The CTA's tiles t_k = blockIdx.x + k * gridDim.x are taken in pairs
+//     (t_2p, t_2p+1); the two tiles' stages are interleaved ((t_2p, 0),
+//     (t_2p+1, 0), (t_2p, 1), ...), and tile t_2p+g goes to promotion group
+//     g through TMEM partial set g.
+//   * warp 16: producer (lane 0).  Per 128-wide K stage it issues four TMA
+//     loads on one barrier: a 128 x 128 A tile, a 64 x 128 B tile, and the
+//     stage's scale boxes sa[4 row tiles][4 K blocks] and sb[2 column
+//     tiles][4 K blocks].  The 8-slot ring is split into two 4-slot rings,
+//     one per tile of the pair.  Nothing on the producer waits for global
+//     memory, so it runs up to four stages ahead on each tile.
+//   * warp 17: MMA issuer (lane 0).  Per stage, four MMAs (M=128, N=64, K=32,
 //     one per 32-wide K block) into the four 64-column TMEM partial buffers
-//     of one of two buffer sets; one commit hands the whole set over.
-//   * warps 0-7: promotion.  Warp w reads TMEM lanes 32(w%4).. (C rows) and
-//     columns 32(w/4)..+31 of each partial, exactly one 32 x 32 scale tile,
-//     so its scale is one number per K block: sa * sb from two 16-byte
-//     shared-memory vectors per stage.  Each thread keeps its row's 32 FP32 accumulators in
-//     registers (as 16 packed pairs) and adds (sa*sb) * partial with packed
-//     FMAs (fma.rn.f32x2), two K blocks' partials per TMEM wait, each pair
-//     of K blocks in one asm statement.  After the last stage of a tile it
-//     rounds to BF16 and stores 64 bytes.
-//   * A stage is recycled once all eight promotion warps have read its
+//     of the stage's group's set; one commit hands the whole set over.
+//   * warps 8g .. 8g+7: promotion group g.  Warp w reads TMEM lanes
+//     32(w%4).. (C rows) and columns 32((w%8)/4)..+31 of each partial of its
+//     set, exactly one 32 x 32 scale tile, so its scale is one number per K
+//     block: sa * sb from two 16-byte shared-memory vectors per stage.  Each
+//     thread keeps its row's 32 FP32 accumulators in registers (as 16 packed
+//     pairs) and adds (sa*sb) * partial with packed FMAs (fma.rn.f32x2), one
+//     K block per asm statement.  After the last stage of a tile it rounds
+//     to BF16 and stores 64 bytes.
+//   * A stage is recycled once the eight warps of its group have read its
 //     scales (empty count 8): they read them only after the stage's partial
 //     set is committed, which implies that the stage's MMAs, the last
-//     readers of its operand tiles, have completed.  A partial-buffer set is
-//     reused once all eight warps hold its data in registers (pempty count
-//     8).
+//     readers of its operand tiles, have completed.  The scale reads are
+//     generic-proxy loads and the slot's next fill is an async-proxy (TMA)
+//     write, so each warp issues fence.proxy.async before it arrives;
+//     without it the next fill's scale boxes were seen to land under the
+//     reads at tile changes.  A partial-buffer set is reused once its eight
+//     warps hold its data in registers (pempty count 8).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -57,10 +68,16 @@ constexpr int KB = 32;           // scale block along K, = K per MMA
 constexpr int KPS = BK / KB;     // K blocks per stage (4)
 constexpr int STAGES = 8;
 constexpr int NSETS = 2;         // TMEM partial-buffer sets, KPS buffers each
-constexpr int kPromoWarps = 8;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kGroups = 2;       // promotion groups: group g uses set g
+// Each group owns its own STAGES / kGroups slots of the stage ring (slot
+// 2i + g), so that a slot's barriers always see the same consumers in the
+// same order, however the two tiles' stages interleave.
+constexpr int SUB = STAGES / kGroups;
+constexpr int kGroupWarps = 8;   // promotion warps per group
+constexpr int kPromoWarps = kGroups * kGroupWarps;
+constexpr int kProducerWarp = kPromoWarps;
+constexpr int kMmaWarp = kPromoWarps + 1;
+constexpr int kThreads = 32 * (kPromoWarps + 2);
 constexpr int GROUP_M = 16;
 constexpr int kTmemCols = NSETS * KPS * BN;  // 512
 
@@ -122,61 +139,53 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n,
   nb = r / gm;
 }
 
-// Promotion of two K blocks' partials (32 columns each, one lane row):
-// loads both from TMEM, waits, and adds s0 * first + s1 * second into the
-// 32 FP32 accumulators held as 16 packed pairs (acc[j] = columns 2j, 2j+1),
-// with packed FMAs fma.rn.f32x2 (each lane of a pair rounded once).  One
-// asm statement, so the loaded values never leave it.
-__device__ __forceinline__ void promote_pair(uint64_t (&acc)[16],
-                                             uint32_t taddr0, uint32_t taddr1,
-                                             float s0, float s1) {
+// Promotion of one K block's partial (32 columns, one lane row): loads it
+// from TMEM, waits, and adds s * partial into the 32 FP32 accumulators held
+// as 16 packed pairs, with packed FMAs.  One asm statement.
+__device__ __forceinline__ void promote_one(uint64_t (&acc)[16], uint32_t taddr,
+                                            float s) {
   asm volatile(
       "{\n\t"
-      ".reg .b32 p<64>;\n\t"
-      ".reg .b64 q<32>, sa, sb;\n\t"
+      ".reg .b32 p<32>;\n\t"
+      ".reg .b64 q<16>, sc;\n\t"
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {p0, p1, p2, p3, p4, p5, p6, p7, p8, p9, p10, p11, p12, p13, p14, p15, p16, p17, p18, p19, p20, p21, p22, p23, p24, p25, p26, p27, p28, p29, p30, p31}, [%16];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {p32, p33, p34, p35, p36, p37, p38, p39, p40, p41, p42, p43, p44, p45, p46, p47, p48, p49, p50, p51, p52, p53, p54, p55, p56, p57, p58, p59, p60, p61, p62, p63}, [%17];\n\t"
       "tcgen05.wait::ld.sync.aligned;\n\t"
-      "mov.b64 sa, {%18, %18};\n\t"
-      "mov.b64 sb, {%19, %19};\n\t"
-      "mov.b64 q0, {p0, p1};\n\tfma.rn.f32x2 %0, sa, q0, %0;\n\t"
-      "mov.b64 q1, {p2, p3};\n\tfma.rn.f32x2 %1, sa, q1, %1;\n\t"
-      "mov.b64 q2, {p4, p5};\n\tfma.rn.f32x2 %2, sa, q2, %2;\n\t"
-      "mov.b64 q3, {p6, p7};\n\tfma.rn.f32x2 %3, sa, q3, %3;\n\t"
-      "mov.b64 q4, {p8, p9};\n\tfma.rn.f32x2 %4, sa, q4, %4;\n\t"
-      "mov.b64 q5, {p10, p11};\n\tfma.rn.f32x2 %5, sa, q5, %5;\n\t"
-      "mov.b64 q6, {p12, p13};\n\tfma.rn.f32x2 %6, sa, q6, %6;\n\t"
-      "mov.b64 q7, {p14, p15};\n\tfma.rn.f32x2 %7, sa, q7, %7;\n\t"
-      "mov.b64 q8, {p16, p17};\n\tfma.rn.f32x2 %8, sa, q8, %8;\n\t"
-      "mov.b64 q9, {p18, p19};\n\tfma.rn.f32x2 %9, sa, q9, %9;\n\t"
-      "mov.b64 q10, {p20, p21};\n\tfma.rn.f32x2 %10, sa, q10, %10;\n\t"
-      "mov.b64 q11, {p22, p23};\n\tfma.rn.f32x2 %11, sa, q11, %11;\n\t"
-      "mov.b64 q12, {p24, p25};\n\tfma.rn.f32x2 %12, sa, q12, %12;\n\t"
-      "mov.b64 q13, {p26, p27};\n\tfma.rn.f32x2 %13, sa, q13, %13;\n\t"
-      "mov.b64 q14, {p28, p29};\n\tfma.rn.f32x2 %14, sa, q14, %14;\n\t"
-      "mov.b64 q15, {p30, p31};\n\tfma.rn.f32x2 %15, sa, q15, %15;\n\t"
-      "mov.b64 q16, {p32, p33};\n\tfma.rn.f32x2 %0, sb, q16, %0;\n\t"
-      "mov.b64 q17, {p34, p35};\n\tfma.rn.f32x2 %1, sb, q17, %1;\n\t"
-      "mov.b64 q18, {p36, p37};\n\tfma.rn.f32x2 %2, sb, q18, %2;\n\t"
-      "mov.b64 q19, {p38, p39};\n\tfma.rn.f32x2 %3, sb, q19, %3;\n\t"
-      "mov.b64 q20, {p40, p41};\n\tfma.rn.f32x2 %4, sb, q20, %4;\n\t"
-      "mov.b64 q21, {p42, p43};\n\tfma.rn.f32x2 %5, sb, q21, %5;\n\t"
-      "mov.b64 q22, {p44, p45};\n\tfma.rn.f32x2 %6, sb, q22, %6;\n\t"
-      "mov.b64 q23, {p46, p47};\n\tfma.rn.f32x2 %7, sb, q23, %7;\n\t"
-      "mov.b64 q24, {p48, p49};\n\tfma.rn.f32x2 %8, sb, q24, %8;\n\t"
-      "mov.b64 q25, {p50, p51};\n\tfma.rn.f32x2 %9, sb, q25, %9;\n\t"
-      "mov.b64 q26, {p52, p53};\n\tfma.rn.f32x2 %10, sb, q26, %10;\n\t"
-      "mov.b64 q27, {p54, p55};\n\tfma.rn.f32x2 %11, sb, q27, %11;\n\t"
-      "mov.b64 q28, {p56, p57};\n\tfma.rn.f32x2 %12, sb, q28, %12;\n\t"
-      "mov.b64 q29, {p58, p59};\n\tfma.rn.f32x2 %13, sb, q29, %13;\n\t"
-      "mov.b64 q30, {p60, p61};\n\tfma.rn.f32x2 %14, sb, q30, %14;\n\t"
-      "mov.b64 q31, {p62, p63};\n\tfma.rn.f32x2 %15, sb, q31, %15;\n\t"
+      "mov.b64 sc, {%17, %17};\n\t"
+      "mov.b64 q0, {p0, p1};\n\t"
+      "mov.b64 q1, {p2, p3};\n\t"
+      "mov.b64 q2, {p4, p5};\n\t"
+      "mov.b64 q3, {p6, p7};\n\t"
+      "mov.b64 q4, {p8, p9};\n\t"
+      "mov.b64 q5, {p10, p11};\n\t"
+      "mov.b64 q6, {p12, p13};\n\t"
+      "mov.b64 q7, {p14, p15};\n\t"
+      "mov.b64 q8, {p16, p17};\n\t"
+      "mov.b64 q9, {p18, p19};\n\t"
+      "mov.b64 q10, {p20, p21};\n\t"
+      "mov.b64 q11, {p22, p23};\n\t"
+      "mov.b64 q12, {p24, p25};\n\t"
+      "mov.b64 q13, {p26, p27};\n\t"
+      "mov.b64 q14, {p28, p29};\n\t"
+      "mov.b64 q15, {p30, p31};\n\t"
+      "fma.rn.f32x2 %0, sc, q0, %0;\n\t"
+      "fma.rn.f32x2 %1, sc, q1, %1;\n\t"
+      "fma.rn.f32x2 %2, sc, q2, %2;\n\t"
+      "fma.rn.f32x2 %3, sc, q3, %3;\n\t"
+      "fma.rn.f32x2 %4, sc, q4, %4;\n\t"
+      "fma.rn.f32x2 %5, sc, q5, %5;\n\t"
+      "fma.rn.f32x2 %6, sc, q6, %6;\n\t"
+      "fma.rn.f32x2 %7, sc, q7, %7;\n\t"
+      "fma.rn.f32x2 %8, sc, q8, %8;\n\t"
+      "fma.rn.f32x2 %9, sc, q9, %9;\n\t"
+      "fma.rn.f32x2 %10, sc, q10, %10;\n\t"
+      "fma.rn.f32x2 %11, sc, q11, %11;\n\t"
+      "fma.rn.f32x2 %12, sc, q12, %12;\n\t"
+      "fma.rn.f32x2 %13, sc, q13, %13;\n\t"
+      "fma.rn.f32x2 %14, sc, q14, %14;\n\t"
+      "fma.rn.f32x2 %15, sc, q15, %15;\n\t"
       "}"
-      : "+l"(acc[0]), "+l"(acc[1]), "+l"(acc[2]), "+l"(acc[3]), "+l"(acc[4]),
-        "+l"(acc[5]), "+l"(acc[6]), "+l"(acc[7]), "+l"(acc[8]), "+l"(acc[9]),
-        "+l"(acc[10]), "+l"(acc[11]), "+l"(acc[12]), "+l"(acc[13]),
-        "+l"(acc[14]), "+l"(acc[15])
-      : "r"(taddr0), "r"(taddr1), "f"(s0), "f"(s1)
+      : "+l"(acc[0]), "+l"(acc[1]), "+l"(acc[2]), "+l"(acc[3]), "+l"(acc[4]), "+l"(acc[5]), "+l"(acc[6]), "+l"(acc[7]), "+l"(acc[8]), "+l"(acc[9]), "+l"(acc[10]), "+l"(acc[11]), "+l"(acc[12]), "+l"(acc[13]), "+l"(acc[14]), "+l"(acc[15])
+      : "r"(taddr), "f"(s)
       : "memory");
 }
 
@@ -208,15 +217,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tiles_n = (a.N + BN - 1) / BN;
   const int total_tiles = tiles_m * tiles_n;
   const int nks = (a.K + BK - 1) / BK;          // stages per tile
+  const int G = gridDim.x;
+  // The CTA's tiles t_k = blockIdx.x + k G are taken in pairs (t_2p,
+  // t_2p+1); the two tiles of a pair are computed together, their stages
+  // interleaved ((t_2p, 0), (t_2p+1, 0), (t_2p, 1), ...), tile t_2p+g by
+  // promotion group g on partial set g.  A pair without a second tile runs
+  // its first tile's stages alone.
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), kPromoWarps);
+      mbar_init(empty_bar(s), kGroupWarps);    // the group that uses it
     }
     for (int p = 0; p < NSETS; ++p) {
       mbar_init(pfull_bar(p), 1);
-      mbar_init(pempty_bar(p), kPromoWarps);
+      mbar_init(pempty_bar(p), kGroupWarps);
     }
     mbar_init(final_bar, 1);
     *abort_flag = 0;
@@ -237,73 +252,90 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // Stage k of group g: ring slot 2 (k % SUB) + g, phase (k / SUB) & 1.
+  auto slot_of = [](int g, uint32_t k) { return 2u * (k % SUB) + g; };
+  auto phase_of = [](uint32_t k) { return (k / SUB) & 1u; };
+
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    uint32_t s = 0, ph = 0, issued = 0;
+    uint32_t kg[kGroups] = {0, 0}, issued = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-      int mb, nb;
-      tile_coords(t, tiles_m, tiles_n, mb, nb);
-      const int m0 = mb * BM, n0 = nb * BN;
-      for (int ks = 0; ks < nks; ++ks) {
-        const bool ready = mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns,
-                                     a.status, abort_flag);
-        if (!__all_sync(0xffffffffu, ready)) {
-          ok = false;
-          break;
+    for (int t0 = blockIdx.x; ok && t0 < total_tiles; t0 += 2 * G) {
+      const int ntile = t0 + G < total_tiles ? 2 : 1;
+      int m0[2], n0[2];
+      for (int g = 0; g < ntile; ++g) {
+        int mb, nb;
+        tile_coords(t0 + g * G, tiles_m, tiles_n, mb, nb);
+        m0[g] = mb * BM;
+        n0[g] = nb * BN;
+      }
+      for (int ks = 0; ok && ks < nks; ++ks) {
+        for (int g = 0; g < ntile; ++g) {
+          const uint32_t s = slot_of(g, kg[g]), ph = phase_of(kg[g]);
+          const bool ready = mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns,
+                                       a.status, abort_flag);
+          if (!__all_sync(0xffffffffu, ready)) {
+            ok = false;
+            break;
+          }
+          // Operand tiles and the stage's scale boxes, all on one barrier.
+          // TMA zero-fills scale entries past the grid's edge.
+          if (lane == 0 && !(a.withhold_first && issued == 0)) {
+            const uint32_t fb = full_bar(s);
+            const uint32_t sslot = base + Lay::kScale + s * Lay::kScaleSlot;
+            mbar_arrive_expect_tx(fb, Lay::kStageBytes);
+            tma_load_2d(base + Lay::kA + s * Lay::kABytes, &tmA, fb, ks * BK, m0[g]);
+            tma_load_2d(base + Lay::kB + s * Lay::kBBytes, &tmB, fb, ks * BK, n0[g]);
+            tma_load_2d(sslot, &tmSa, fb, ks * KPS, m0[g] / 32);
+            tma_load_2d(sslot + Lay::kSbOffset, &tmSb, fb, ks * KPS, n0[g] / 32);
+          }
+          ++issued;
+          ++kg[g];
         }
-        // Operand tiles and the stage's scale boxes, all on one barrier.
-        // TMA zero-fills scale entries past the grid's edge.
-        if (lane == 0 && !(a.withhold_first && issued == 0)) {
-          const uint32_t fb = full_bar(s);
-          const uint32_t sslot = base + Lay::kScale + s * Lay::kScaleSlot;
-          mbar_arrive_expect_tx(fb, Lay::kStageBytes);
-          tma_load_2d(base + Lay::kA + s * Lay::kABytes, &tmA, fb, ks * BK, m0);
-          tma_load_2d(base + Lay::kB + s * Lay::kBBytes, &tmB, fb, ks * BK, n0);
-          tma_load_2d(sslot, &tmSa, fb, ks * KPS, m0 / 32);
-          tma_load_2d(sslot + Lay::kSbOffset, &tmSb, fb, ks * KPS, n0 / 32);
-        }
-        ++issued;
-        if (++s == STAGES) { s = 0; ph ^= 1u; }
       }
     }
     if (lane == 0) {
-      for (uint32_t st = 0; st < STAGES; ++st) {
-        if (issued <= st) break;
-        const uint32_t arms = (issued - 1 - st) / STAGES + 1;
-        if (a.withhold_first && st == 0 && arms == 1) continue;  // never armed
-        mbar_wait_drain(full_bar(st), (arms - 1) & 1u, a.timeout_ns, a.status);
-      }
+      for (int g = 0; g < kGroups; ++g)
+        for (uint32_t i = 0; i < SUB; ++i) {
+          if (kg[g] <= i) break;
+          const uint32_t arms = (kg[g] - 1 - i) / SUB + 1;
+          if (a.withhold_first && g == 0 && i == 0 && arms == 1) continue;  // never armed
+          mbar_wait_drain(full_bar(slot_of(g, i)), (arms - 1) & 1u,
+                          a.timeout_ns, a.status);
+        }
     }
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
-      uint32_t s = 0, ph = 0, set = 0, sph = 0;
+      uint32_t use[NSETS] = {0, 0};   // stages of each group = uses of its set
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+      for (int t0 = blockIdx.x; ok && t0 < total_tiles; t0 += 2 * G) {
+        const int ntile = t0 + G < total_tiles ? 2 : 1;
         for (int ks = 0; ok && ks < nks; ++ks) {
-          if (!mbar_wait(full_bar(s), ph, a.timeout_ns, a.status,
-                         abort_flag) ||
-              !mbar_wait(pempty_bar(set), sph ^ 1u, a.timeout_ns, a.status,
-                         abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t adesc =
-              smem_desc_k128_sw128(base + Lay::kA + s * Lay::kABytes);
-          const uint64_t bdesc =
-              smem_desc_k128_sw128(base + Lay::kB + s * Lay::kBBytes);
+          for (int g = 0; ok && g < ntile; ++g) {
+            const uint32_t s = slot_of(g, use[g]), ph = phase_of(use[g]);
+            if (!mbar_wait(full_bar(s), ph, a.timeout_ns, a.status,
+                           abort_flag) ||
+                !mbar_wait(pempty_bar(g), (use[g] & 1u) ^ 1u, a.timeout_ns,
+                           a.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t adesc =
+                smem_desc_k128_sw128(base + Lay::kA + s * Lay::kABytes);
+            const uint64_t bdesc =
+                smem_desc_k128_sw128(base + Lay::kB + s * Lay::kBBytes);
 #pragma unroll
-          for (int k = 0; k < KPS; ++k)
-            umma_f8f6f4(tmem_base + (set * KPS + k) * BN, adesc + 2u * k,
-                        bdesc + 2u * k, idesc, 0u);
-          // No commit for the stage itself: its promotion warps release it
-          // after this set's commit, which implies these MMAs are done.
-          umma_commit(pfull_bar(set));
-          if (++set == NSETS) { set = 0; sph ^= 1u; }
-          if (++s == STAGES) { s = 0; ph ^= 1u; }
+            for (int k = 0; k < KPS; ++k)
+              umma_f8f6f4(tmem_base + (g * KPS + k) * BN, adesc + 2u * k,
+                          bdesc + 2u * k, idesc, 0u);
+            // No commit for the stage itself: its promotion warps release
+            // it after this set's commit, which implies these MMAs are done.
+            umma_commit(pfull_bar(g));
+            ++use[g];
+          }
         }
       }
       umma_commit(final_bar);
@@ -311,25 +343,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ----------------------------------------------------------- promotion
+    const int grp = warp / kGroupWarps;          // which tile of a pair
+    const int gw = warp % kGroupWarps;
     const int q = warp & 3;          // TMEM lane quarter = 32-row tile
-    const int c = warp >> 2;         // 32-column slice = column tile
+    const int c = gw >> 2;           // 32-column slice = column tile
     const uint32_t col0 = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                          32 * c;
-    uint32_t s = 0, ph = 0, set = 0, sph = 0;
+                          32 * c + grp * KPS * BN;
+    uint32_t use = 0;                // this group's stages = uses of its set
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+    for (int t0 = blockIdx.x; ok && t0 < total_tiles; t0 += 2 * G) {
+      const int ntile = t0 + G < total_tiles ? 2 : 1;
+      if (grp >= ntile) continue;    // no second tile in this pair
+      const int t = t0 + grp * G;
       int mb, nb;
       tile_coords(t, tiles_m, tiles_n, mb, nb);
       uint64_t acc[16];   // packed FP32 pairs: columns 2j, 2j+1
 #pragma unroll
       for (int j = 0; j < 16; ++j) acc[j] = 0;
-      for (int ks = 0; ok && ks < nks; ++ks) {
+      for (int ks = 0; ok && ks < nks; ++ks, ++use) {
+        const uint32_t s = slot_of(grp, use), ph = phase_of(use);
         // Scale products of this stage (acquired through the stage's full
-        // barrier), then let the stage go as far as this warp is concerned.
+        // barrier), then let the stage go as far as this group is concerned.
         const bool sready = mbar_wait(full_bar(s), ph, a.timeout_ns,
                                       a.status, abort_flag);
         const bool pready = sready &&
-                            mbar_wait(pfull_bar(set), sph, a.timeout_ns,
+                            mbar_wait(pfull_bar(grp), use & 1u, a.timeout_ns,
                                       a.status, abort_flag);
         if (!__all_sync(0xffffffffu, sready && pready)) {
           ok = false;
@@ -342,19 +380,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             c * KPS * 4);
         const float4 sc = make_float4(__fmul_rn(va.x, vb.x), __fmul_rn(va.y, vb.y),
                                       __fmul_rn(va.z, vb.z), __fmul_rn(va.w, vb.w));
+        // Order these generic reads before the TMA writes of the slot's next
+        // fill, which the arrival below lets the producer issue.
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(s));
-        if (++s == STAGES) { s = 0; ph ^= 1u; }
         tc_fence_after();
-        const uint32_t pbase = col0 + set * KPS * BN;
-        // K blocks 0 and 1, then 2 and 3; after the second pair the whole
-        // set is in registers and goes back to the MMA warp.
-        promote_pair(acc, pbase, pbase + BN, sc.x, sc.y);
-        promote_pair(acc, pbase + 2 * BN, pbase + 3 * BN, sc.z, sc.w);
+        promote_one(acc, col0, sc.x);
+        promote_one(acc, col0 + BN, sc.y);
+        promote_one(acc, col0 + 2 * BN, sc.z);
+        promote_one(acc, col0 + 3 * BN, sc.w);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(pempty_bar(set));
-        if (++set == NSETS) { set = 0; sph ^= 1u; }
+        if (lane == 0) mbar_arrive(pempty_bar(grp));
       }
       if (!ok) break;
       // Epilogue: round to BF16 and store this thread's 32 columns.

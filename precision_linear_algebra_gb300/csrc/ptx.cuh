@@ -153,8 +153,10 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-// Orders this thread's generic-proxy shared-memory writes before later
-// async-proxy (TMA) reads of them.
+// Orders this thread's generic-proxy shared-memory accesses before later
+// async-proxy (TMA) accesses: writes before TMA reads of them (a TMA store
+// from a staging buffer), and reads before TMA writes over them (a ring slot
+// refilled once its readers release it).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
