@@ -90,6 +90,28 @@ def test_many_tiles_per_cta_all_outputs():
     assert frac > 0.98
 
 
+def test_tile_pairs_and_ring_laps_all_outputs():
+    """Four 128 x 64 tiles per persistent CTA (two pairs of tiles computed
+    together) and K = 1344 (42 scale blocks, 10.5 stages, so every ring
+    slot is refilled several times per tile), every output checked.  Scales
+    read from a ring slot after its next fill had landed (a stage's scales
+    replaced by those four stages later) showed only after a CTA's first
+    pair of tiles.
+    The race depended on timing (one call in three failed), so three calls
+    are checked."""
+    fl = lib()
+    M, N, K = 1024, 4864, 1344
+    rng = np.random.default_rng(78)
+    A, B = random_codes(rng, (M, K)), random_codes(rng, (N, K))
+    sa, sb = _scales(rng, M, K), _scales(rng, N, K)
+    r, Cref = oracle.gemm_blockscaled_32x32(A, B, sa, sb)
+    bound = oracle.tolerance_blockscaled_32x32(A, B, sa, sb, r)
+    for call in range(3):
+        got = _run(fl, A, B, sa, sb)
+        assert_within_bound(got, r, bound, "tile pairs, call %d" % call)
+        assert np.mean(got == oracle.bf16_bits_to_float(Cref)) > 0.98
+
+
 def test_equal_scales_match_pertensor_bound():
     fl = lib()
     rng = np.random.default_rng(2)
