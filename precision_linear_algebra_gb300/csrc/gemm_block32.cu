@@ -20,22 +20,21 @@
 // 128 FP32 lanes per SM versus 8192 tensor FMAs per clock this caps the
 // kernel near half the dense FP8 peak.  What holds it below that is the
 // latency of each handoff between the MMA warp and the promotion warps, so
-// the CTA works on two output tiles at once and gives each its own
-// promotion group, which hides one group's waits behind the other's FMAs;
-// all synchronisation is at the granularity of 128-wide K stages:
-//   * The CTA's tiles t_k = blockIdx.x + k * gridDim.x are taken in pairs
-//     (t_2p, t_2p+1); the two tiles' stages are interleaved ((t_2p, 0),
-//     (t_2p+1, 0), (t_2p, 1), ...), and tile t_2p+g goes to promotion group
-//     g through TMEM partial set g.
-//   * warp 16: producer (lane 0).  Per 128-wide K stage it issues four TMA
-//     loads on one barrier: a 128 x 128 A tile, a 64 x 128 B tile, and the
-//     stage's scale boxes sa[4 row tiles][4 K blocks] and sb[2 column
-//     tiles][4 K blocks].  The 8-slot ring is split into two 4-slot rings,
-//     one per tile of the pair.  Nothing on the producer waits for global
-//     memory, so it runs up to four stages ahead on each tile.
-//   * warp 17: MMA issuer (lane 0).  Per stage, four MMAs (M=128, N=64, K=32,
-//     one per 32-wide K block) into the four 64-column TMEM partial buffers
-//     of the stage's group's set; one commit hands the whole set over.
+// the CTA's 128 x 128 tile is split into two 128 x 64 halves, each with its
+// own TMEM partial set and its own promotion group, which hides one group's
+// waits behind the other's FMAs; all synchronisation is at the granularity
+// of 128-wide K stages:
+//   * warp 16: producer (lane 0).  Per 128-wide K stage (7-stage ring) it
+//     issues four TMA loads on one barrier: a 128 x 128 A tile, a 128 x 128
+//     B tile (both halves' columns), and the stage's scale boxes sa[4 row
+//     tiles][4 K blocks] and sb[4 column tiles][4 K blocks].  The two
+//     halves share the stage's A tile.  Nothing on the producer waits for
+//     global memory, so it runs up to seven stages ahead.
+//   * warp 17: MMA issuer (lane 0).  Per stage and half g, four MMAs (M=128,
+//     N=64, K=32, one per 32-wide K block; B = rows 64g.. of the stage's B
+//     tile) into the four 64-column TMEM partial buffers of set g; one
+//     commit hands the whole set to group g.  Half 0 is issued before half
+//     1, so the two groups run about half a stage apart.
 //   * warps 8g .. 8g+7: promotion group g.  Warp w reads TMEM lanes
 //     32(w%4).. (C rows) and columns 32((w%8)/4)..+31 of each partial of its
 //     set, exactly one 32 x 32 scale tile, so its scale is one number per K
@@ -44,10 +43,10 @@
 //     pairs) and adds (sa*sb) * partial with packed FMAs (fma.rn.f32x2), one
 //     K block per asm statement.  After the last stage of a tile it rounds
 //     to BF16 and stores 64 bytes.
-//   * A stage is recycled once the eight warps of its group have read its
-//     scales (empty count 8): they read them only after the stage's partial
-//     set is committed, which implies that the stage's MMAs, the last
-//     readers of its operand tiles, have completed.  The scale reads are
+//   * A stage is recycled once all sixteen promotion warps have read its
+//     scales (empty count 16): each group reads them only after its set for
+//     the stage is committed, which implies that its MMAs, readers of the
+//     stage's operand tiles, have completed.  The scale reads are
 //     generic-proxy loads and the slot's next fill is an async-proxy (TMA)
 //     write, so each warp issues fence.proxy.async before it arrives;
 //     without it the next fill's scale boxes were seen to land under the
@@ -62,17 +61,14 @@ namespace fp8la {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 64;
+constexpr int BN = 64;           // columns of one group's half tile
+constexpr int BNS = 2 * BN;      // columns of a CTA tile (two halves)
 constexpr int BK = 128;          // K per stage (bytes = E4M3 values)
 constexpr int KB = 32;           // scale block along K, = K per MMA
 constexpr int KPS = BK / KB;     // K blocks per stage (4)
-constexpr int STAGES = 8;
+constexpr int STAGES = 7;
 constexpr int NSETS = 2;         // TMEM partial-buffer sets, KPS buffers each
 constexpr int kGroups = 2;       // promotion groups: group g uses set g
-// Each group owns its own STAGES / kGroups slots of the stage ring (slot
-// 2i + g), so that a slot's barriers always see the same consumers in the
-// same order, however the two tiles' stages interleave.
-constexpr int SUB = STAGES / kGroups;
 constexpr int kGroupWarps = 8;   // promotion warps per group
 constexpr int kPromoWarps = kGroups * kGroupWarps;
 constexpr int kProducerWarp = kPromoWarps;
@@ -97,14 +93,14 @@ struct BsArgs {
 
 struct Lay {
   static constexpr int kABytes = BM * BK;
-  static constexpr int kBBytes = BN * BK;
+  static constexpr int kBBytes = BNS * BK;
   static constexpr int kSaBytes = 4 * KPS * 4;
-  static constexpr int kSbBytes = 2 * KPS * 4;
+  static constexpr int kSbBytes = 4 * KPS * 4;
   static constexpr int kStageBytes = kABytes + kBBytes + kSaBytes + kSbBytes;
   static constexpr int kA = 0;
   static constexpr int kB = kA + STAGES * kABytes;
   // Per stage: the A-scale box [4 row tiles][4 K blocks] (64 B) at +0 and
-  // the B-scale box [2 column tiles][4 K blocks] (32 B) at +128.  Every TMA
+  // the B-scale box [4 column tiles][4 K blocks] (64 B) at +128.  Every TMA
   // destination in shared memory starts on a 128-byte boundary.
   static constexpr int kSbOffset = 128;
   static constexpr int kScaleSlot = 256;
@@ -214,20 +210,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       reinterpret_cast<volatile int *>(sbase + Lay::kMisc + 4);
 
   const int tiles_m = (a.M + BM - 1) / BM;
-  const int tiles_n = (a.N + BN - 1) / BN;
+  const int tiles_n = (a.N + BNS - 1) / BNS;    // tiles of 128 columns
   const int total_tiles = tiles_m * tiles_n;
   const int nks = (a.K + BK - 1) / BK;          // stages per tile
-  const int G = gridDim.x;
-  // The CTA's tiles t_k = blockIdx.x + k G are taken in pairs (t_2p,
-  // t_2p+1); the two tiles of a pair are computed together, their stages
-  // interleaved ((t_2p, 0), (t_2p+1, 0), (t_2p, 1), ...), tile t_2p+g by
-  // promotion group g on partial set g.  A pair without a second tile runs
-  // its first tile's stages alone.
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), kGroupWarps);    // the group that uses it
+      mbar_init(empty_bar(s), kPromoWarps);     // both groups read it
     }
     for (int p = 0; p < NSETS; ++p) {
       mbar_init(pfull_bar(p), 1);
@@ -252,90 +242,79 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // Stage k of group g: ring slot 2 (k % SUB) + g, phase (k / SUB) & 1.
-  auto slot_of = [](int g, uint32_t k) { return 2u * (k % SUB) + g; };
-  auto phase_of = [](uint32_t k) { return (k / SUB) & 1u; };
-
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    uint32_t kg[kGroups] = {0, 0}, issued = 0;
+    uint32_t s = 0, ph = 0, issued = 0;
     bool ok = true;
-    for (int t0 = blockIdx.x; ok && t0 < total_tiles; t0 += 2 * G) {
-      const int ntile = t0 + G < total_tiles ? 2 : 1;
-      int m0[2], n0[2];
-      for (int g = 0; g < ntile; ++g) {
-        int mb, nb;
-        tile_coords(t0 + g * G, tiles_m, tiles_n, mb, nb);
-        m0[g] = mb * BM;
-        n0[g] = nb * BN;
-      }
-      for (int ks = 0; ok && ks < nks; ++ks) {
-        for (int g = 0; g < ntile; ++g) {
-          const uint32_t s = slot_of(g, kg[g]), ph = phase_of(kg[g]);
-          const bool ready = mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns,
-                                       a.status, abort_flag);
-          if (!__all_sync(0xffffffffu, ready)) {
-            ok = false;
-            break;
-          }
-          // Operand tiles and the stage's scale boxes, all on one barrier.
-          // TMA zero-fills scale entries past the grid's edge.
-          if (lane == 0 && !(a.withhold_first && issued == 0)) {
-            const uint32_t fb = full_bar(s);
-            const uint32_t sslot = base + Lay::kScale + s * Lay::kScaleSlot;
-            mbar_arrive_expect_tx(fb, Lay::kStageBytes);
-            tma_load_2d(base + Lay::kA + s * Lay::kABytes, &tmA, fb, ks * BK, m0[g]);
-            tma_load_2d(base + Lay::kB + s * Lay::kBBytes, &tmB, fb, ks * BK, n0[g]);
-            tma_load_2d(sslot, &tmSa, fb, ks * KPS, m0[g] / 32);
-            tma_load_2d(sslot + Lay::kSbOffset, &tmSb, fb, ks * KPS, n0[g] / 32);
-          }
-          ++issued;
-          ++kg[g];
+    for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+      int mb, nb;
+      tile_coords(t, tiles_m, tiles_n, mb, nb);
+      const int m0 = mb * BM, n0 = nb * BNS;
+      for (int ks = 0; ks < nks; ++ks) {
+        const bool ready = mbar_wait(empty_bar(s), ph ^ 1u, a.timeout_ns,
+                                     a.status, abort_flag);
+        if (!__all_sync(0xffffffffu, ready)) {
+          ok = false;
+          break;
         }
+        // Operand tiles and the stage's scale boxes, all on one barrier.
+        // TMA zero-fills scale entries past the grid's edge.
+        if (lane == 0 && !(a.withhold_first && issued == 0)) {
+          const uint32_t fb = full_bar(s);
+          const uint32_t sslot = base + Lay::kScale + s * Lay::kScaleSlot;
+          mbar_arrive_expect_tx(fb, Lay::kStageBytes);
+          tma_load_2d(base + Lay::kA + s * Lay::kABytes, &tmA, fb, ks * BK, m0);
+          tma_load_2d(base + Lay::kB + s * Lay::kBBytes, &tmB, fb, ks * BK, n0);
+          tma_load_2d(sslot, &tmSa, fb, ks * KPS, m0 / 32);
+          tma_load_2d(sslot + Lay::kSbOffset, &tmSb, fb, ks * KPS, n0 / 32);
+        }
+        ++issued;
+        if (++s == STAGES) { s = 0; ph ^= 1u; }
       }
     }
+    // Wait for the copies this warp armed before the CTA may exit.
     if (lane == 0) {
-      for (int g = 0; g < kGroups; ++g)
-        for (uint32_t i = 0; i < SUB; ++i) {
-          if (kg[g] <= i) break;
-          const uint32_t arms = (kg[g] - 1 - i) / SUB + 1;
-          if (a.withhold_first && g == 0 && i == 0 && arms == 1) continue;  // never armed
-          mbar_wait_drain(full_bar(slot_of(g, i)), (arms - 1) & 1u,
-                          a.timeout_ns, a.status);
-        }
+      for (uint32_t st = 0; st < STAGES; ++st) {
+        if (issued <= st) break;
+        const uint32_t arms = (issued - 1 - st) / STAGES + 1;
+        if (a.withhold_first && st == 0 && arms == 1) continue;  // never armed
+        mbar_wait_drain(full_bar(st), (arms - 1) & 1u, a.timeout_ns, a.status);
+      }
     }
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
-      uint32_t use[NSETS] = {0, 0};   // stages of each group = uses of its set
+      uint32_t s = 0, ph = 0, use = 0;  // stage ring; uses of each set
       bool ok = true;
-      for (int t0 = blockIdx.x; ok && t0 < total_tiles; t0 += 2 * G) {
-        const int ntile = t0 + G < total_tiles ? 2 : 1;
-        for (int ks = 0; ok && ks < nks; ++ks) {
-          for (int g = 0; ok && g < ntile; ++g) {
-            const uint32_t s = slot_of(g, use[g]), ph = phase_of(use[g]);
-            if (!mbar_wait(full_bar(s), ph, a.timeout_ns, a.status,
-                           abort_flag) ||
-                !mbar_wait(pempty_bar(g), (use[g] & 1u) ^ 1u, a.timeout_ns,
+      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        for (int ks = 0; ok && ks < nks; ++ks, ++use) {
+          if (!mbar_wait(full_bar(s), ph, a.timeout_ns, a.status,
+                         abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint64_t adesc =
+              smem_desc_k128_sw128(base + Lay::kA + s * Lay::kABytes);
+          for (int g = 0; g < kGroups; ++g) {
+            if (!mbar_wait(pempty_bar(g), (use & 1u) ^ 1u, a.timeout_ns,
                            a.status, abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint64_t adesc =
-                smem_desc_k128_sw128(base + Lay::kA + s * Lay::kABytes);
-            const uint64_t bdesc =
-                smem_desc_k128_sw128(base + Lay::kB + s * Lay::kBBytes);
+            // Group g's half of the B tile: rows 64 g .. 64 g + 63.
+            const uint64_t bdesc = smem_desc_k128_sw128(
+                base + Lay::kB + s * Lay::kBBytes + g * BN * BK);
 #pragma unroll
             for (int k = 0; k < KPS; ++k)
               umma_f8f6f4(tmem_base + (g * KPS + k) * BN, adesc + 2u * k,
                           bdesc + 2u * k, idesc, 0u);
-            // No commit for the stage itself: its promotion warps release
-            // it after this set's commit, which implies these MMAs are done.
+            // The stage's shared memory is released by both groups after
+            // their sets' commits, which imply the stage's MMAs are done.
             umma_commit(pfull_bar(g));
-            ++use[g];
           }
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
       }
       umma_commit(final_bar);
@@ -343,27 +322,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ----------------------------------------------------------- promotion
-    const int grp = warp / kGroupWarps;          // which tile of a pair
+    const int grp = warp / kGroupWarps;          // which half of the tile
     const int gw = warp % kGroupWarps;
     const int q = warp & 3;          // TMEM lane quarter = 32-row tile
-    const int c = gw >> 2;           // 32-column slice = column tile
+    const int c = gw >> 2;           // 32-column slice within the half
     const uint32_t col0 = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                           32 * c + grp * KPS * BN;
-    uint32_t use = 0;                // this group's stages = uses of its set
+    uint32_t s = 0, ph = 0, use = 0;
     bool ok = true;
-    for (int t0 = blockIdx.x; ok && t0 < total_tiles; t0 += 2 * G) {
-      const int ntile = t0 + G < total_tiles ? 2 : 1;
-      if (grp >= ntile) continue;    // no second tile in this pair
-      const int t = t0 + grp * G;
+    for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
       int mb, nb;
       tile_coords(t, tiles_m, tiles_n, mb, nb);
       uint64_t acc[16];   // packed FP32 pairs: columns 2j, 2j+1
 #pragma unroll
       for (int j = 0; j < 16; ++j) acc[j] = 0;
       for (int ks = 0; ok && ks < nks; ++ks, ++use) {
-        const uint32_t s = slot_of(grp, use), ph = phase_of(use);
         // Scale products of this stage (acquired through the stage's full
-        // barrier), then let the stage go as far as this group is concerned.
+        // barrier), then let the stage go as far as this warp is concerned.
         const bool sready = mbar_wait(full_bar(s), ph, a.timeout_ns,
                                       a.status, abort_flag);
         const bool pready = sready &&
@@ -377,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             sbase + Lay::kScale + s * Lay::kScaleSlot + q * KPS * 4);
         const float4 vb = *reinterpret_cast<const float4 *>(
             sbase + Lay::kScale + s * Lay::kScaleSlot + Lay::kSbOffset +
-            c * KPS * 4);
+            (2 * grp + c) * KPS * 4);
         const float4 sc = make_float4(__fmul_rn(va.x, vb.x), __fmul_rn(va.y, vb.y),
                                       __fmul_rn(va.z, vb.z), __fmul_rn(va.w, vb.w));
         // Order these generic reads before the TMA writes of the slot's next
@@ -385,6 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(s));
+        if (++s == STAGES) { s = 0; ph ^= 1u; }
         tc_fence_after();
         promote_one(acc, col0, sc.x);
         promote_one(acc, col0 + BN, sc.y);
@@ -397,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       // Epilogue: round to BF16 and store this thread's 32 columns.
       const int row = mb * BM + q * 32 + lane;
-      const int n = nb * BN + 32 * c;
+      const int n = nb * BNS + grp * BN + 32 * c;
       if (row < a.M && n < a.N) {
         uint16_t *crow = a.C + static_cast<int64_t>(row) * a.ldc;
         uint32_t w[16];
@@ -512,9 +488,9 @@ fp8la_status blockscaled_impl(const uint8_t *A, int64_t lda, const uint8_t *B,
   if (!device_is_sm10x()) return FP8LA_ERR_UNSUPPORTED;
   CUtensorMap tmA, tmB, tmSa, tmSb;
   if (!encode_2d_bs(&tmA, A, K, M, lda, BK, BM) ||
-      !encode_2d_bs(&tmB, B, K, N, ldb, BK, BN) ||
+      !encode_2d_bs(&tmB, B, K, N, ldb, BK, BNS) ||
       !encode_2d_f32(&tmSa, sa, nkb, (M + 31) / 32, ld_sa * 4, KPS, BM / 32) ||
-      !encode_2d_f32(&tmSb, sb, nkb, (N + 31) / 32, ld_sb * 4, KPS, BN / 32))
+      !encode_2d_f32(&tmSb, sb, nkb, (N + 31) / 32, ld_sb * 4, KPS, BNS / 32))
     return FP8LA_ERR_CUDA;
   unsigned *status = status_word_ptr();
   if (!status) return FP8LA_ERR_CUDA;
@@ -540,7 +516,7 @@ fp8la_status blockscaled_impl(const uint8_t *A, int64_t lda, const uint8_t *B,
     return FP8LA_ERR_CUDA;
   const int sms = sm_count();
   if (sms <= 0) return FP8LA_ERR_CUDA;
-  const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int64_t tiles = ((M + BM - 1) / BM) * ((N + BNS - 1) / BNS);
   const int grid = static_cast<int>(tiles < sms ? tiles : sms);
   gemm_e4m3_block32_kernel<<<grid, kThreads, Lay::kAlloc, s>>>(tmA, tmB, tmSa,
                                                                tmSb, args);

@@ -91,16 +91,15 @@ def test_many_tiles_per_cta_all_outputs():
 
 
 def test_tile_pairs_and_ring_laps_all_outputs():
-    """Four 128 x 64 tiles per persistent CTA (two pairs of tiles computed
-    together) and K = 1344 (42 scale blocks, 10.5 stages, so every ring
-    slot is refilled several times per tile), every output checked.  Scales
-    read from a ring slot after its next fill had landed (a stage's scales
-    replaced by those four stages later) showed only after a CTA's first
-    pair of tiles.
-    The race depended on timing (one call in three failed), so three calls
-    are checked."""
+    """Three 128 x 128 output tiles per persistent CTA (six of 128 x 64) and
+    K = 1344 (42 scale blocks, 10.5 stages of 128, so every ring slot is
+    refilled several times per tile), every output checked.  Scales read
+    from a ring slot after its next fill had landed (a stage's scales
+    replaced by those of a later stage) showed only after a CTA's first
+    tiles.  That race depended on timing (one call in three failed), so
+    three calls are checked."""
     fl = lib()
-    M, N, K = 1024, 4864, 1344
+    M, N, K = 1024, 7296, 1344
     rng = np.random.default_rng(78)
     A, B = random_codes(rng, (M, K)), random_codes(rng, (N, K))
     sa, sb = _scales(rng, M, K), _scales(rng, N, K)
