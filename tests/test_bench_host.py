@@ -1,7 +1,10 @@
 """Host-side rules of the benchmark: a timed region whose clock record shows
 a hardware or thermal slowdown, or SM clocks stuck far below their maximum
 with no reason active, is invalid (it is taken again), while the power cap
-alone is not; and the per-step median and minimum of a kernel's times."""
+alone is not; the clock record keeps the samples taken inside the timed
+region; the sustained peak rates a region that lasts seconds or ran under
+the power cap, the burst peak any other; and the per-step median and
+minimum of a kernel's times."""
 
 import os
 import sys
@@ -41,3 +44,40 @@ def test_median_min_per_step():
     assert bench._median_min_per_step(xs, 3) == [7.0, 3.0]
     assert bench._median_min_per_step([], 3) is None
     assert bench._median_min_per_step([1.0, 2.0], 3) is None
+
+
+def _row(t, sm, reasons=(), mx="2070"):
+    flags = ["Active" if r in reasons else "Not Active" for r in bench._CLOCK_REASONS]
+    return [t, "0", str(sm), mx, "900.0", "0x0"] + flags
+
+
+def test_clock_summary_keeps_the_timed_region():
+    rows = [_row(10.0, 2070), _row(10.1, 2070), _row(10.6, 1500, ["sw_power_cap"]),
+            _row(10.7, 1520, ["sw_power_cap"]), _row(11.5, 2070)]
+    c = bench._summarise_clocks(rows, window=(10.55, 10.75))
+    assert c["samples_in_timed_region"] == 2 and c["window"] == "timed region"
+    assert c["sm_mhz"] == 1510.0 and c["reasons"] == ["sw_power_cap"]
+    # a region shorter than the sampling interval: every sample counts
+    c = bench._summarise_clocks(rows, window=(10.3, 10.31))
+    assert c["samples_in_timed_region"] == 0 and c["samples"] == 5
+    assert c["sm_mhz"] == 2070.0 and c["reasons"] == ["sw_power_cap"]
+    # no window: every sample, and no window fields
+    assert "window" not in bench._summarise_clocks(rows)
+
+
+def test_nvsmi_timestamps_parse():
+    t = bench._parse_nvsmi_time("2026/12/03 07:25:22.250")
+    assert t is not None and abs(t % 1 - 0.25) < 1e-6
+    assert bench._parse_nvsmi_time("n/a") is None
+
+
+def test_peak_regime():
+    capped = _c(["sw_power_cap"], sm=1777.0)
+    assert bench._peak_regime(420.0, capped, True, False)[0]
+    assert bench._peak_regime(2500.0, _c([]), True, False)[0]
+    # short, unthrottled regions, graph replays and a missing sustained
+    # figure are rated against the burst figure
+    assert not bench._peak_regime(8.0, _c([]), True, False)[0]
+    assert not bench._peak_regime(8.0, _c(["sw_power_cap"], sm=2060.0), True, False)[0]
+    assert not bench._peak_regime(420.0, capped, True, True)[0]
+    assert not bench._peak_regime(420.0, capped, False, False)[0]
