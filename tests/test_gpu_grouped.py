@@ -91,7 +91,10 @@ def test_grouped_equals_per_group_gemm_calls(variant):
 def test_moe_layer_full_size_sampled(variant):
     """8 experts, K 4096, N 14336, 16384 routed rows with Dirichlet counts;
     per-expert per-tensor quantisation on the GPU, one grouped launch; the
-    oracle checks sampled rows of every group against sampled columns."""
+    oracle checks sampled rows of every group against sampled columns, and
+    every row of each group's first and last 256-row blocks (the last one
+    partial, computed transposed by the CTA-pair kernel) against a
+    contiguous 512-column block."""
     import torch
     fl = lib()
     counts, offs, X, W = workloads.moe_layer(seed=0)
@@ -128,6 +131,16 @@ def test_moe_layer_full_size_sampled(variant):
         rows = np.sort(rng.choice(hi - lo, min(48, hi - lo), replace=False))
         check_pertensor(Cn[lo + rows][:, cols], qx_n[lo:hi], qw_n[e], sx_n[e], sw_n[e],
                         rows=rows, cols=cols, what="expert %d" % e)
+        n_rows = hi - lo
+        last0 = (n_rows - 1) // 256 * 256
+        rblk = np.unique(np.concatenate([np.arange(min(256, n_rows)),
+                                         np.arange(last0, n_rows)]))
+        c0 = int(rng.integers(0, N // 256 - 1)) * 256
+        cblk = np.arange(c0, c0 + 512)
+        assert np.array_equal(qw_n[e][cblk], oracle.encode((W[e][cblk] * qs).astype(np.float32)))
+        check_pertensor(Cn[lo + rblk][:, cblk], qx_n[lo:hi], qw_n[e], sx_n[e], sw_n[e],
+                        rows=rblk, cols=cblk,
+                        what="expert %d, first and last row blocks" % e)
 
 
 def _launch_raw(fl, E, d_off, cap, dA, kp, dB, N, dC, ldc, K, d_sa, d_sb):
