@@ -818,21 +818,67 @@ def _workload_grouped(fl, torch, dev, sptr, ph):
     P = lambda t, i=0: t.data_ptr() + i * t.element_size()
     offs_l = [int(v) for v in offs]
 
-    def step():
-        ph.mark("quant")
+    # Codes and scales are double-buffered for the pipelined schedule.
+    qx2 = [qx, torch.empty_like(qx)]
+    qw2 = [qw, torch.empty_like(qw)]
+    amax2 = [amax, torch.empty_like(amax)]
+    sx2 = [sx, torch.empty_like(sx)]
+    sw2 = [sw, torch.empty_like(sw)]
+
+    def quant(b, s):
         for e in range(E):
             lo, hi = offs_l[e], offs_l[e + 1]
-            fl.fp8_quantize_pertensor(P(X) + lo * K * 4, hi - lo, K, K, P(qx) + lo * K, K,
-                                      P(amax, e), P(sx, e), sptr)
-            fl.fp8_quantize_pertensor(P(W) + e * N * K * 4, N, K, K, P(qw) + e * N * K, K,
-                                      P(amax, E + e), P(sw, e), sptr)
+            fl.fp8_quantize_pertensor(P(X) + lo * K * 4, hi - lo, K, K, P(qx2[b]) + lo * K, K,
+                                      P(amax2[b], e), P(sx2[b], e), s)
+            fl.fp8_quantize_pertensor(P(W) + e * N * K * 4, N, K, K, P(qw2[b]) + e * N * K, K,
+                                      P(amax2[b], E + e), P(sw2[b], e), s)
+
+    def gemm(b, s):
+        fl.fp8_grouped_gemm(E, d_off.data_ptr(), Mt, P(qx2[b]), K, P(qw2[b]), K, N * K, P(C),
+                            N, N, K, P(sx2[b]), P(sw2[b]), s)
+
+    def step():
+        ph.mark("quant")
+        quant(0, sptr)
         ph.mark("quant")
         ph.mark("gemm")
-        fl.fp8_grouped_gemm(E, d_off.data_ptr(), Mt, P(qx), K, P(qw), K, N * K, P(C), N, N, K,
-                            P(sx), P(sw), sptr)
+        gemm(0, sptr)
         ph.mark("gemm")
 
-    return dict(step=step, flops=2.0 * Mt * N * K, launches=4 * E + 1,
+    # Pipelined schedule, as for the 8192^3 workload: step i+1's
+    # quantisation on one stream while step i's grouped GEMM runs on another;
+    # events order quantize(i) before GEMM(i) and GEMM(i) before
+    # quantize(i+2), which reuses its buffers.
+    main = torch.cuda.current_stream(dev)
+    sq, sg = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    qdone = [torch.cuda.Event(), torch.cuda.Event()]
+    gdone = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def pbegin():
+        for ev in qdone + gdone:
+            ev.record(main)
+        sq.wait_stream(main)
+        sg.wait_stream(main)
+
+    def pstep(i):
+        b = i & 1
+        sq.wait_event(gdone[b])
+        ph.mark("quant", sq)
+        quant(b, sq.cuda_stream)
+        ph.mark("quant", sq)
+        qdone[b].record(sq)
+        sg.wait_event(qdone[b])
+        ph.mark("gemm", sg)
+        gemm(b, sg.cuda_stream)
+        ph.mark("gemm", sg)
+        gdone[b].record(sg)
+
+    def pend():
+        main.wait_stream(sq)
+        main.wait_stream(sg)
+
+    return dict(step=step, pipeline=(pbegin, pstep, pend), flops=2.0 * Mt * N * K,
+                launches=4 * E + 1,
                 workload=("grouped MoE E4M3: 8 experts, K 4096, N 14336, 8192 tokens top-2 "
                           "(16384 rows, Dirichlet(1) counts %s), per-expert per-tensor quantize "
                           "of activations and weights, one grouped GEMM launch; seed 0"
