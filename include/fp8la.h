@@ -80,7 +80,8 @@ typedef int fp8la_status;
 #define FP8LA_ERR_CUDA           -4  /* a CUDA runtime or driver call failed */
 #define FP8LA_ERR_DEVICE_TIMEOUT -5  /* a bounded wait inside a kernel ran out */
 #define FP8LA_ERR_DEVICE_ARG     -6  /* a kernel found a device-side argument it
-                                        cannot use (fp8_grouped_gemm m_offsets) */
+                                        cannot use (m_offsets of fp8_grouped_gemm or
+                                        fp8_quantize_pertensor_grouped) */
 
 /*
  * Per-tensor E4M3 quantisation ([P1] risks paragraph: E4M3 spans +-448 and
@@ -204,6 +205,39 @@ FP8LA_API fp8la_status fp8_gemm_ex(const uint8_t *A, int64_t lda,
                                    const float *scale_a, const float *scale_b,
                                    int32_t a_format, int32_t b_format,
                                    fp8la_stream_t stream);
+
+/*
+ * Grouped per-tensor E4M3 quantisation: the per-expert operand feed of
+ * fp8_grouped_gemm ([P3] implementation paragraph: the MoE grouped GEMM;
+ * [P1] risks paragraph: per-tensor scaling).  Group e, the rows r in
+ * [m_offsets[e], m_offsets[e+1]) of x, is quantised as fp8_quantize_pertensor
+ * quantises a tensor, with its own amax:
+ *
+ *   amax_out[e]  = max |x[r][j]| over the group's rows, NaN ignored
+ *   scale_out[e] = fp32(amax_out[e] / 448)   (amax 0 or 448/amax not finite: 1)
+ *   q[r][j]      = E4M3 code of fp32(x[r][j] * fp32(448 / amax_out[e])),
+ *                  round-to-nearest-even, saturating
+ *
+ * m_offsets: int32 [num_groups + 1] on the DEVICE, as for fp8_grouped_gemm
+ * (starting at 0, non-decreasing, m_offsets[num_groups] <= rows_capacity);
+ * the host never reads it, so a routing result can feed the quantiser and
+ * the GEMM without a synchronisation.  Both kernels check it first: offsets
+ * that break these rules make the call write no codes and no scales and
+ * record FP8LA_ERR_DEVICE_ARG in the device status word
+ * (fp8_get_device_status); amax_out is cleared in any case.  Groups with no
+ * rows get amax 0 and scale 1.  x: fp32 [rows_capacity][ldx]; q: uint8
+ * [rows_capacity][ldq] (rows at or past m_offsets[num_groups] are neither
+ * read nor written); amax_out, scale_out: fp32 [num_groups], two arrays that
+ * must not overlap (FP8LA_ERR_INVALID_ARG).  Requires ldx >= cols,
+ * ldq >= cols, 0 <= num_groups <= 1024 (0: nothing is done),
+ * rows_capacity < 2^31.
+ */
+FP8LA_API fp8la_status fp8_quantize_pertensor_grouped(const float *x, int32_t num_groups,
+                                            const int32_t *m_offsets,
+                                            int64_t rows_capacity, int64_t cols,
+                                            int64_t ldx, uint8_t *q, int64_t ldq,
+                                            float *amax_out, float *scale_out,
+                                            fp8la_stream_t stream);
 
 /*
  * 32x32 block-scaled E4M3 GEMM ([P3] implementation paragraph: 32x32 scale

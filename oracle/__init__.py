@@ -41,7 +41,8 @@ from .e4m3 import decode_code, decode, encode, E4M3_MAX, NAN_CODE
 from . import e5m2
 from .bf16 import bf16_rne, bf16_bits_to_float
 from .quantize import (amax_fp32, scales_from_amax, quantize_pertensor,
-                       quantize_pertensor_delayed, quantize_blockwise_32x32)
+                       quantize_pertensor_delayed, quantize_blockwise_32x32,
+                       quantize_pertensor_grouped)
 from .gemm import (gemm_pertensor, gemm_blockscaled_32x32, gemm_grouped,
                    bound_pertensor, bound_blockscaled_32x32, max_abs_decoded,
                    max_abs_tile_scaled_32x32, tolerance_pertensor,
@@ -51,7 +52,7 @@ __all__ = [
     "decode_code", "decode", "encode", "E4M3_MAX", "NAN_CODE", "e5m2",
     "bf16_rne", "bf16_bits_to_float",
     "amax_fp32", "scales_from_amax", "quantize_pertensor",
-    "quantize_blockwise_32x32",
+    "quantize_blockwise_32x32", "quantize_pertensor_grouped",
     "gemm_pertensor", "gemm_blockscaled_32x32", "gemm_grouped",
     "bound_pertensor", "bound_blockscaled_32x32", "max_abs_decoded",
     "max_abs_tile_scaled_32x32", "tolerance_pertensor",

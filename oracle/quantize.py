@@ -112,3 +112,31 @@ def quantize_blockwise_32x32(x):
             codes[rs, cs] = q
             scales[i, j] = s
     return codes, scales
+
+
+def quantize_pertensor_grouped(x, m_offsets):
+    """Per-tensor quantisation of each row group of a 2-D fp32 array.
+
+    Group e is rows m_offsets[e] .. m_offsets[e+1]-1 of x (one MoE expert's
+    tokens, [P3] implementation paragraph: the grouped GEMM for MoE), and is
+    quantised exactly as ``quantize_pertensor`` quantises a whole tensor,
+    with its own amax and scale; a group with no rows has amax 0 and scale 1
+    (steps 1 and 2 on an empty tensor).  Rows at or past m_offsets[E] belong
+    to no group.
+
+    Returns (codes uint8 [m_offsets[E]][C], amax fp32 [E], scale fp32 [E]).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    offs = [int(v) for v in m_offsets]
+    E = len(offs) - 1
+    if x.ndim != 2 or offs[0] != 0 or any(b < a for a, b in zip(offs, offs[1:])) \
+            or offs[-1] > x.shape[0]:
+        raise ValueError("m_offsets must start at 0, not decrease and fit the rows of x")
+    codes = np.empty((offs[-1], x.shape[1]), dtype=np.uint8)
+    amax = np.empty(E, dtype=np.float32)
+    scale = np.empty(E, dtype=np.float32)
+    for e in range(E):
+        q, amax[e], scale[e] = quantize_pertensor(x[offs[e]:offs[e + 1]])
+        codes[offs[e]:offs[e + 1]] = q
+    return codes, amax, scale
+

@@ -39,6 +39,8 @@ SIGNATURES = [
     ("fp8_quantize_pertensor_delayed", _S,
      [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _I32, _P]),
     ("fp8_quantize_blockwise_32x32", _S, [_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P]),
+    ("fp8_quantize_pertensor_grouped", _S,
+     [_P, _I32, _P, _I64, _I64, _I64, _P, _I64, _P, _P, _P]),
     ("fp8_gemm", _S, [_P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P, _P]),
     ("fp8_gemm_ex", _S, [_P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P, _I32, _I32, _P]),
     ("fp8_gemm_blockscaled_32x32", _S,
@@ -123,6 +125,12 @@ def fp8_gemm_ex(A, lda, B, ldb, C, ldc, M, N, K, scale_a, scale_b, a_fmt, b_fmt,
 def fp8_quantize_blockwise_32x32(x, rows, cols, ldx, q, ldq, scales, ld_scales, stream):
     return _call("fp8_quantize_blockwise_32x32", x, rows, cols, ldx, q, ldq,
                  scales, ld_scales, stream)
+
+
+def fp8_quantize_pertensor_grouped(x, num_groups, m_offsets, rows_capacity, cols, ldx, q, ldq,
+                                   amax_out, scale_out, stream):
+    return _call("fp8_quantize_pertensor_grouped", x, num_groups, m_offsets, rows_capacity,
+                 cols, ldx, q, ldq, amax_out, scale_out, stream)
 
 
 def fp8_gemm(A, lda, B, ldb, C, ldc, M, N, K, scale_a, scale_b, stream):
@@ -253,6 +261,27 @@ def quantize_blockwise_32x32(x, q=None, scales=None):
     fp8_quantize_blockwise_32x32(_ptr(x), rows, cols, _ld(x), _ptr(q), _ld(q),
                                  _ptr(scales), _ld(scales), _stream())
     return q, scales
+
+
+def quantize_pertensor_grouped(x, m_offsets, q=None, amax=None, scale=None):
+    """x: fp32 CUDA [rows_capacity][cols]; m_offsets: int32 CUDA [E+1].
+
+    Group e (rows m_offsets[e] .. m_offsets[e+1]-1) is quantised with its own
+    per-tensor amax and scale.  Returns (q uint8 [rows_capacity][cols],
+    amax fp32 [E], scale fp32 [E]); nothing is synchronised.
+    """
+    import torch
+    assert x.dtype == torch.float32 and x.dim() == 2 and x.stride(1) == 1
+    assert m_offsets.dtype == torch.int32 and m_offsets.dim() == 1
+    rows, cols = x.shape
+    E = m_offsets.numel() - 1
+    if q is None:
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    amax = torch.empty(E, dtype=torch.float32, device=x.device) if amax is None else amax
+    scale = torch.empty(E, dtype=torch.float32, device=x.device) if scale is None else scale
+    fp8_quantize_pertensor_grouped(_ptr(x), E, _ptr(m_offsets), rows, cols, _ld(x), _ptr(q),
+                                   _ld(q), _ptr(amax), _ptr(scale), _stream())
+    return q, amax, scale
 
 
 def gemm(A, B, scale_a, scale_b, C=None, a_fmt="e4m3", b_fmt="e4m3"):

@@ -648,10 +648,176 @@ fp8la_status quantize_delayed_impl(const float *x, int64_t rows, int64_t cols,
   return launch_status();
 }
 
+// ------------------------------------------- grouped per-tensor (MoE rows)
+// Rows m_offsets[e] .. m_offsets[e+1]-1 of x form group e (an expert's
+// tokens), quantised with their own per-tensor amax and scale.  The offsets
+// stay on the device; both passes read them into shared memory, check them
+// (m_offsets[0] == 0, non-decreasing, m_offsets[E] <= the row capacity) and
+// on failure record kStatusBadDeviceArg and write nothing.  The work is
+// split into items of kGroupChunkRows rows of one group; item i belongs to
+// the group whose item range [pref[g], pref[g+1]) holds it.
+constexpr int kGroupChunkRows = 8;
+constexpr int kQuantMaxGroups = 1024;
+
+struct GroupTable {
+  int32_t offs[kQuantMaxGroups + 1];
+  int32_t pref[kQuantMaxGroups + 1];
+  int bad;
+};
+
+// Fills `t` from m_offsets (all threads of the block take part); returns
+// false for offsets that fail the check.
+__device__ bool load_group_table(GroupTable &t, const int32_t *m_offsets,
+                                 int E, int64_t rows_cap) {
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) t.offs[e] = m_offsets[e];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int bad = t.offs[0] != 0 || t.offs[E] > rows_cap;
+    int32_t acc = 0;
+    for (int e = 0; e < E; ++e) {
+      const int32_t n = t.offs[e + 1] - t.offs[e];
+      if (n < 0) bad = 1;
+      t.pref[e] = acc;
+      acc += n > 0 ? (n + kGroupChunkRows - 1) / kGroupChunkRows : 0;
+    }
+    t.pref[E] = acc;
+    t.bad = bad;
+  }
+  __syncthreads();
+  return !t.bad;
+}
+
+// The group of work item i (pref[g] <= i < pref[g+1]; empty groups have
+// an empty range).
+__device__ __forceinline__ int group_of_item(const GroupTable &t, int E,
+                                             int32_t i) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (t.pref[mid] <= i) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(kThreads, kMinBlocksBound)
+    amax_grouped_kernel(const float *__restrict__ x, int64_t ldx,
+                        int64_t cols, const int32_t *m_offsets, int E,
+                        int64_t rows_cap, float *amax_out, unsigned *status) {
+  __shared__ GroupTable t;
+  if (!load_group_table(t, m_offsets, E, rows_cap)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, kStatusBadDeviceArg);
+    return;
+  }
+  const int64_t units = VEC == 4 ? cols / 4 : cols;
+  for (int32_t i = blockIdx.x; i < t.pref[E]; i += gridDim.x) {
+    const int g = group_of_item(t, E, i);
+    const int64_t r0 = t.offs[g] + static_cast<int64_t>(i - t.pref[g]) * kGroupChunkRows;
+    const int64_t r1 = min(r0 + kGroupChunkRows, static_cast<int64_t>(t.offs[g + 1]));
+    float m = 0.0f;
+#pragma unroll 4
+    for (int64_t r = r0; r < r1; ++r) {
+      if (VEC == 4) {
+        const float4 *row = reinterpret_cast<const float4 *>(x + r * ldx);
+        for (int64_t c = threadIdx.x; c < units; c += blockDim.x)
+          m = max_abs4(m, ld_stream4(row + c));
+      } else {
+        const float *row = x + r * ldx;
+        for (int64_t c = threadIdx.x; c < units; c += blockDim.x)
+          m = fmaxf(m, fabsf(row[c]));
+      }
+    }
+    block_max_into(m, amax_out + g);
+    __syncthreads();   // block_max_into's shared buffer is reused next item
+  }
+}
+
+template <int VEC, int FMT>
+__global__ void __launch_bounds__(kThreads, kMinBlocksBound)
+    cast_grouped_kernel(const float *__restrict__ x, int64_t ldx, int64_t cols,
+                        uint8_t *__restrict__ q, int64_t ldq,
+                        const int32_t *m_offsets, int E, int64_t rows_cap,
+                        const float *amax_in, float *scale_out,
+                        unsigned *status) {
+  __shared__ GroupTable t;
+  if (!load_group_table(t, m_offsets, E, rows_cap)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, kStatusBadDeviceArg);
+    return;
+  }
+  // Every group's scale, empty groups included, from block 0.
+  if (blockIdx.x == 0)
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+      scale_out[e] = scales_from_amax<FMT>(amax_in[e]).scale;
+  const int64_t units = VEC == 4 ? cols / 4 : cols;
+  for (int32_t i = blockIdx.x; i < t.pref[E]; i += gridDim.x) {
+    const int g = group_of_item(t, E, i);
+    const int64_t r0 = t.offs[g] + static_cast<int64_t>(i - t.pref[g]) * kGroupChunkRows;
+    const int64_t r1 = min(r0 + kGroupChunkRows, static_cast<int64_t>(t.offs[g + 1]));
+    const float qs = scales_from_amax<FMT>(amax_in[g]).qscale;
+#pragma unroll 4
+    for (int64_t r = r0; r < r1; ++r) {
+      if (VEC == 4) {
+        const float4 *row = reinterpret_cast<const float4 *>(x + r * ldx);
+        uint32_t *qrow = reinterpret_cast<uint32_t *>(q + r * ldq);
+        for (int64_t c = threadIdx.x; c < units; c += blockDim.x)
+          qrow[c] = cvt4<FMT>(ld_stream4(row + c), qs);
+      } else {
+        const float *row = x + r * ldx;
+        uint8_t *qrow = q + r * ldq;
+        for (int64_t c = threadIdx.x; c < units; c += blockDim.x)
+          qrow[c] = cvt1<FMT>(row[c], qs);
+      }
+    }
+  }
+}
+
+fp8la_status quantize_grouped_impl(const float *x, int32_t E,
+                                   const int32_t *m_offsets, int64_t rows_cap,
+                                   int64_t cols, int64_t ldx, uint8_t *q,
+                                   int64_t ldq, float *amax_out,
+                                   float *scale_out, cudaStream_t s) {
+  if (E < 0 || E > kQuantMaxGroups || rows_cap < 0 || cols < 0)
+    return FP8LA_ERR_INVALID_ARG;
+  if (E == 0) return FP8LA_OK;
+  if (!m_offsets || !amax_out || !scale_out) return FP8LA_ERR_INVALID_ARG;
+  // The cast blocks read amax_out while block 0 writes scale_out.
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(amax_out);
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(scale_out);
+  const uintptr_t bytes = static_cast<uintptr_t>(E) * sizeof(float);
+  if (a0 < s0 + bytes && s0 < a0 + bytes) return FP8LA_ERR_INVALID_ARG;
+  if (rows_cap > 0 && cols > 0 && (!x || !q || ldx < cols || ldq < cols))
+    return FP8LA_ERR_INVALID_ARG;
+  if (rows_cap >= (int64_t(1) << 31) || cols > (int64_t(1) << 40))
+    return FP8LA_ERR_UNSUPPORTED;
+  if (sm_count() <= 0) return FP8LA_ERR_CUDA;
+  unsigned *status = status_word_ptr();
+  if (!status) return FP8LA_ERR_CUDA;
+  if (cudaMemsetAsync(amax_out, 0, bytes, s) != cudaSuccess) return FP8LA_ERR_CUDA;
+  const bool vec4 = cols % 4 == 0 && ldx % 4 == 0 && ldq % 4 == 0 &&
+                    aligned16(x) && (reinterpret_cast<uintptr_t>(q) & 3u) == 0;
+  // Items: at most rows_cap / kGroupChunkRows + E of them.
+  const int64_t items = (rows_cap + kGroupChunkRows - 1) / kGroupChunkRows + E;
+  const int g = grid_for(items * kThreads, kThreads);
+  const int64_t c = cols > 0 ? cols : 0;
+  if (vec4) {
+    amax_grouped_kernel<4><<<g, kThreads, 0, s>>>(x, ldx, c, m_offsets, E,
+                                                  rows_cap, amax_out, status);
+    cast_grouped_kernel<4, 0><<<g, kThreads, 0, s>>>(
+        x, ldx, c, q, ldq, m_offsets, E, rows_cap, amax_out, scale_out, status);
+  } else {
+    amax_grouped_kernel<1><<<g, kThreads, 0, s>>>(x, ldx, c, m_offsets, E,
+                                                  rows_cap, amax_out, status);
+    cast_grouped_kernel<1, 0><<<g, kThreads, 0, s>>>(
+        x, ldx, c, q, ldq, m_offsets, E, rows_cap, amax_out, scale_out, status);
+  }
+  return launch_status();
+}
+
 }  // namespace
 }  // namespace fp8la
 
 extern "C" fp8la_status fp8_quantize_pertensor(const float *x, int64_t rows,
+
                                                int64_t cols, int64_t ldx,
                                                uint8_t *q, int64_t ldq,
                                                float *amax_out,
@@ -714,4 +880,13 @@ extern "C" fp8la_status fp8_quantize_pertensor_delayed(
     return quantize_delayed_impl<1>(x, rows, cols, ldx, q, ldq, amax_prev,
                                     amax_out, scale_out, s);
   return FP8LA_ERR_INVALID_ARG;
+}
+
+extern "C" fp8la_status fp8_quantize_pertensor_grouped(
+    const float *x, int32_t num_groups, const int32_t *m_offsets,
+    int64_t rows_capacity, int64_t cols, int64_t ldx, uint8_t *q, int64_t ldq,
+    float *amax_out, float *scale_out, fp8la_stream_t stream) {
+  return quantize_grouped_impl(x, num_groups, m_offsets, rows_capacity, cols,
+                               ldx, q, ldq, amax_out, scale_out,
+                               reinterpret_cast<cudaStream_t>(stream));
 }

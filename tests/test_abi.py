@@ -93,6 +93,16 @@ def test_host_argument_rejection(lib):
     assert lib.fp8_grouped_gemm(0, one, 8, one, 16, one, 16, 256, one, 8, 8, 16, one, one, None) == -1
     assert lib.fp8_grouped_gemm(2000, one, 8, one, 16, one, 16, 256, one, 8, 8, 16, one, one, None) == -1
     assert lib.fp8_grouped_gemm(2, None, 8, one, 16, one, 16, 256, one, 8, 8, 16, one, one, None) == -1
+    # grouped quantiser: group count out of range, NULL offsets, ld < cols,
+    # overlapping amax and scale arrays; no groups is a no-op
+    qg = lib.fp8_quantize_pertensor_grouped
+    assert qg(one, -1, one, 8, 4, 4, one, 4, P(64), P(128), None) == -1
+    assert qg(one, 1025, one, 8, 4, 4, one, 4, P(64), P(128), None) == -1
+    assert qg(one, 2, None, 8, 4, 4, one, 4, P(64), P(128), None) == -1
+    assert qg(one, 2, one, 8, 8, 4, one, 8, P(64), P(128), None) == -1
+    assert qg(one, 4, one, 8, 4, 4, one, 4, P(64), P(72), None) == -1    # 16 B vs 8 B apart
+    assert qg(one, 4, one, 8, 4, 4, one, 4, P(72), P(64), None) == -1
+    assert qg(None, 0, None, 0, 4, 4, None, 4, None, None, None) == 0
     # timeout setter
     assert lib.fp8la_set_wait_timeout_ns(10) == -1
     assert lib.fp8la_set_wait_timeout_ns(2_000_000_000) == 0
