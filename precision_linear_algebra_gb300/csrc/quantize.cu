@@ -659,15 +659,24 @@ fp8la_status quantize_delayed_impl(const float *x, int64_t rows, int64_t cols,
 constexpr int kGroupChunkRows = 8;
 constexpr int kQuantMaxGroups = 1024;
 
+// The offsets and each group's first item, in dynamic shared memory sized
+// for the call's group count (2 (E + 1) words: a few bytes for a handful of
+// experts, so that the quantiser's blocks still fit beside a GEMM's).
 struct GroupTable {
-  int32_t offs[kQuantMaxGroups + 1];
-  int32_t pref[kQuantMaxGroups + 1];
-  int bad;
+  int32_t *offs;   // [E + 1]
+  int32_t *pref;   // [E + 1]
+  int *bad;
 };
+
+__device__ __forceinline__ GroupTable group_table(int E) {
+  extern __shared__ int32_t gt_words[];
+  __shared__ int gt_bad;
+  return GroupTable{gt_words, gt_words + E + 1, &gt_bad};
+}
 
 // Fills `t` from m_offsets (all threads of the block take part); returns
 // false for offsets that fail the check.
-__device__ bool load_group_table(GroupTable &t, const int32_t *m_offsets,
+__device__ bool load_group_table(const GroupTable &t, const int32_t *m_offsets,
                                  int E, int64_t rows_cap) {
   for (int e = threadIdx.x; e <= E; e += blockDim.x) t.offs[e] = m_offsets[e];
   __syncthreads();
@@ -681,10 +690,10 @@ __device__ bool load_group_table(GroupTable &t, const int32_t *m_offsets,
       acc += n > 0 ? (n + kGroupChunkRows - 1) / kGroupChunkRows : 0;
     }
     t.pref[E] = acc;
-    t.bad = bad;
+    *t.bad = bad;
   }
   __syncthreads();
-  return !t.bad;
+  return !*t.bad;
 }
 
 // The group of work item i (pref[g] <= i < pref[g+1]; empty groups have
@@ -704,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksBound)
     amax_grouped_kernel(const float *__restrict__ x, int64_t ldx,
                         int64_t cols, const int32_t *m_offsets, int E,
                         int64_t rows_cap, float *amax_out, unsigned *status) {
-  __shared__ GroupTable t;
+  const GroupTable t = group_table(E);
   if (!load_group_table(t, m_offsets, E, rows_cap)) {
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, kStatusBadDeviceArg);
     return;
@@ -739,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksBound)
                         const int32_t *m_offsets, int E, int64_t rows_cap,
                         const float *amax_in, float *scale_out,
                         unsigned *status) {
-  __shared__ GroupTable t;
+  const GroupTable t = group_table(E);
   if (!load_group_table(t, m_offsets, E, rows_cap)) {
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, kStatusBadDeviceArg);
     return;
@@ -799,15 +808,16 @@ fp8la_status quantize_grouped_impl(const float *x, int32_t E,
   const int64_t items = (rows_cap + kGroupChunkRows - 1) / kGroupChunkRows + E;
   const int g = grid_for(items * kThreads, kThreads);
   const int64_t c = cols > 0 ? cols : 0;
+  const size_t table = 2 * (static_cast<size_t>(E) + 1) * sizeof(int32_t);
   if (vec4) {
-    amax_grouped_kernel<4><<<g, kThreads, 0, s>>>(x, ldx, c, m_offsets, E,
-                                                  rows_cap, amax_out, status);
-    cast_grouped_kernel<4, 0><<<g, kThreads, 0, s>>>(
+    amax_grouped_kernel<4><<<g, kThreads, table, s>>>(x, ldx, c, m_offsets, E,
+                                                      rows_cap, amax_out, status);
+    cast_grouped_kernel<4, 0><<<g, kThreads, table, s>>>(
         x, ldx, c, q, ldq, m_offsets, E, rows_cap, amax_out, scale_out, status);
   } else {
-    amax_grouped_kernel<1><<<g, kThreads, 0, s>>>(x, ldx, c, m_offsets, E,
-                                                  rows_cap, amax_out, status);
-    cast_grouped_kernel<1, 0><<<g, kThreads, 0, s>>>(
+    amax_grouped_kernel<1><<<g, kThreads, table, s>>>(x, ldx, c, m_offsets, E,
+                                                      rows_cap, amax_out, status);
+    cast_grouped_kernel<1, 0><<<g, kThreads, table, s>>>(
         x, ldx, c, q, ldq, m_offsets, E, rows_cap, amax_out, scale_out, status);
   }
   return launch_status();
