@@ -656,7 +656,7 @@ fp8la_status quantize_delayed_impl(const float *x, int64_t rows, int64_t cols,
 // on failure record kStatusBadDeviceArg and write nothing.  The work is
 // split into items of kGroupChunkRows rows of one group; item i belongs to
 // the group whose item range [pref[g], pref[g+1]) holds it.
-constexpr int kGroupChunkRows = 8;
+constexpr int kGroupChunkRows = 4;
 constexpr int kQuantMaxGroups = 1024;
 
 // The offsets and each group's first item, in dynamic shared memory sized
@@ -723,17 +723,31 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksBound)
     const int g = group_of_item(t, E, i);
     const int64_t r0 = t.offs[g] + static_cast<int64_t>(i - t.pref[g]) * kGroupChunkRows;
     const int64_t r1 = min(r0 + kGroupChunkRows, static_cast<int64_t>(t.offs[g + 1]));
+    const int nr = static_cast<int>(r1 - r0);
     float m = 0.0f;
-#pragma unroll 4
-    for (int64_t r = r0; r < r1; ++r) {
+    // A thread takes a column of the item's rows: up to kGroupChunkRows
+    // independent loads in flight.
+    for (int64_t c = threadIdx.x; c < units; c += blockDim.x) {
       if (VEC == 4) {
-        const float4 *row = reinterpret_cast<const float4 *>(x + r * ldx);
-        for (int64_t c = threadIdx.x; c < units; c += blockDim.x)
-          m = max_abs4(m, ld_stream4(row + c));
+        const float4 *col = reinterpret_cast<const float4 *>(x + r0 * ldx) + c;
+        const int64_t ld4 = ldx / 4;
+        if (nr == kGroupChunkRows) {
+          // a whole item: all its loads in flight before the first use
+          float4 v[kGroupChunkRows];
+#pragma unroll
+          for (int k = 0; k < kGroupChunkRows; ++k) v[k] = ld_stream4(col + k * ld4);
+#pragma unroll
+          for (int k = 0; k < kGroupChunkRows; ++k) m = max_abs4(m, v[k]);
+        } else {
+          for (int k = 0; k < nr; ++k) m = max_abs4(m, ld_stream4(col + k * ld4));
+        }
       } else {
-        const float *row = x + r * ldx;
-        for (int64_t c = threadIdx.x; c < units; c += blockDim.x)
-          m = fmaxf(m, fabsf(row[c]));
+        const float *col = x + r0 * ldx + c;
+        float v[kGroupChunkRows];
+#pragma unroll
+        for (int k = 0; k < kGroupChunkRows; ++k) v[k] = k < nr ? col[k * ldx] : 0.0f;
+#pragma unroll
+        for (int k = 0; k < kGroupChunkRows; ++k) m = fmaxf(m, fabsf(v[k]));
       }
     }
     block_max_into(m, amax_out + g);
@@ -763,18 +777,33 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksBound)
     const int64_t r0 = t.offs[g] + static_cast<int64_t>(i - t.pref[g]) * kGroupChunkRows;
     const int64_t r1 = min(r0 + kGroupChunkRows, static_cast<int64_t>(t.offs[g + 1]));
     const float qs = scales_from_amax<FMT>(amax_in[g]).qscale;
-#pragma unroll 4
-    for (int64_t r = r0; r < r1; ++r) {
+    const int nr = static_cast<int>(r1 - r0);
+    for (int64_t c = threadIdx.x; c < units; c += blockDim.x) {
       if (VEC == 4) {
-        const float4 *row = reinterpret_cast<const float4 *>(x + r * ldx);
-        uint32_t *qrow = reinterpret_cast<uint32_t *>(q + r * ldq);
-        for (int64_t c = threadIdx.x; c < units; c += blockDim.x)
-          qrow[c] = cvt4<FMT>(ld_stream4(row + c), qs);
+        const float4 *col = reinterpret_cast<const float4 *>(x + r0 * ldx) + c;
+        uint32_t *qcol = reinterpret_cast<uint32_t *>(q + r0 * ldq) + c;
+        const int64_t ld4 = ldx / 4, ldq4 = ldq / 4;
+        if (nr == kGroupChunkRows) {
+          // a whole item: all its loads in flight before the first store
+          float4 v[kGroupChunkRows];
+#pragma unroll
+          for (int k = 0; k < kGroupChunkRows; ++k) v[k] = ld_stream4(col + k * ld4);
+#pragma unroll
+          for (int k = 0; k < kGroupChunkRows; ++k) qcol[k * ldq4] = cvt4<FMT>(v[k], qs);
+        } else {
+          for (int k = 0; k < nr; ++k)
+            qcol[k * ldq4] = cvt4<FMT>(ld_stream4(col + k * ld4), qs);
+        }
       } else {
-        const float *row = x + r * ldx;
-        uint8_t *qrow = q + r * ldq;
-        for (int64_t c = threadIdx.x; c < units; c += blockDim.x)
-          qrow[c] = cvt1<FMT>(row[c], qs);
+        const float *col = x + r0 * ldx + c;
+        uint8_t *qcol = q + r0 * ldq + c;
+        float v[kGroupChunkRows];
+#pragma unroll
+        for (int k = 0; k < kGroupChunkRows; ++k)
+          if (k < nr) v[k] = col[k * ldx];
+#pragma unroll
+        for (int k = 0; k < kGroupChunkRows; ++k)
+          if (k < nr) qcol[k * ldq] = cvt1<FMT>(v[k], qs);
       }
     }
   }
