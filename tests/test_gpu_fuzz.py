@@ -188,3 +188,31 @@ def test_quantisers_random_shapes(case):
     rqb, rsb = oracle.quantize_blockwise_32x32(x)
     assert np.array_equal(qb.cpu().numpy(), rqb), (rows, cols, pad)
     assert np.array_equal(sb.cpu().numpy(), rsb), (rows, cols, pad)
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_grouped_quantiser_random_shapes(case):
+    """Grouped per-tensor quantisation of random ragged groups (some empty)
+    with padded strides and guard rows past the last group, bit for bit."""
+    import torch
+    fl = lib()
+    rng = np.random.default_rng(5000 + case)
+    E = int(rng.integers(1, 17))
+    counts = rng.integers(0, 200, E) * (rng.random(E) > 0.3)
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    rows, cols = int(offs[-1]), int(rng.integers(1, 900))
+    cap = rows + int(rng.integers(0, 20))
+    pad = int(rng.integers(0, 9))
+    x = (rng.standard_normal((rows, cols)) * 10.0 ** rng.uniform(-4, 4)).astype(np.float32)
+    dfull = torch.zeros((cap, cols + pad), dtype=torch.float32, device="cuda")
+    dfull[:rows, :cols] = to_dev(x)
+    qfull = torch.full((cap, cols + pad), 0xA5, dtype=torch.uint8, device="cuda")
+    d_off = to_dev(offs)
+    q, amax, scale = fl.quantize_pertensor_grouped(dfull[:, :cols], d_off, q=qfull[:, :cols])
+    torch.cuda.synchronize()
+    assert fl.device_status() == 0
+    rq, ramax, rscale = oracle.quantize_pertensor_grouped(x, offs)
+    got = qfull.cpu().numpy()
+    assert np.array_equal(got[:rows, :cols], rq), (E, rows, cols, pad)
+    assert np.array_equal(amax.cpu().numpy(), ramax) and np.array_equal(scale.cpu().numpy(), rscale)
+    assert np.all(got[rows:] == 0xA5) and np.all(got[:, cols:] == 0xA5)
