@@ -40,8 +40,9 @@ constexpr int kMinBlocksBound = 3;
 constexpr int kBlock32PerSm = 4;
 // Bytes of x's tail that the amax pass asks L2 to keep for the cast pass
 // (L2 is 129 MB; the rest of it holds the codes being written and other
-// work's data).
-constexpr int64_t kL2KeepBytes = int64_t(64) << 20;
+// work's data).  96 MB measured 1.5 % faster than 64 MB for an 8192 x 8192
+// operand, 112 MB no faster than 96.
+constexpr int64_t kL2KeepBytes = int64_t(96) << 20;
 
 // FP8 formats: 0 = E4M3 (max 448), 1 = E5M2 (max 57344).
 template <int FMT>
