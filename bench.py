@@ -200,6 +200,29 @@ class ClockSampler:
         return _summarise_clocks(self.rows, window)
 
 
+def _alu_promotion_peak(torch, dev):
+    """Ceiling of the 32x32 block-scaled GEMM on the CUDA cores, in GEMM
+    TFLOP/s: each output needs one FP32 FMA per 32-wide K block (64 GEMM
+    FLOP per FMA), at 128 FP32 FMAs per SM per clock (four sub-partitions of
+    32 lanes; a packed fma.rn.f32x2 issues at half the rate, so it does not
+    raise this), on every SM at the maximum SM clock."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f).get("sm_max_mhz"))
+    except Exception:
+        pass
+    src = "MEASURED_PEAKS.json sm_max_mhz"
+    if not mhz:
+        mhz, src = 2070.0, "the maximum SM clock of the part"
+    peak = 64.0 * 128 * sms * mhz * 1e6 / 1e12
+    return peak, ("CUDA-core promotion ceiling: 128 FP32 FMA per SM per clock x %d SMs x "
+                  "%.0f MHz (%s) x 64 GEMM FLOP per FMA (one FMA per output per 32-wide "
+                  "K block); the tensor-core work of the same GEMM takes half as long"
+                  % (sms, mhz, src))
+
+
 def _peak_regime(ms_total, clocks, have_sustained, graph_replayed):
     """Which measured peak rates the dominant kernel of a timed region:
     (True, why) for the sustained figure -- it comes from a seconds-long
@@ -786,7 +809,7 @@ def _workload_blockscaled(fl, torch, dev, sptr, ph, linears=("qkv", "attn_out", 
                                           sw.data_ptr(), sw.stride(0), sptr)
             ph.mark("gemm")
 
-    return dict(step=step, flops=flops, launches=12, quant_bytes_per_elem=5,
+    return dict(step=step, flops=flops, launches=12, quant_bytes_per_elem=5, gemm_bound="alu",
                 workload=("32x32 block-scaled E4M3: block-quantize activations [4096][K] ~ N(0,1) "
                           "and weights [N][K] ~ N(0,0.02), then the block-scaled GEMM, for the "
                           "four 70B-class linears qkv (10240,8192), attn_out (8192,8192), gate_up "
@@ -1175,6 +1198,7 @@ def run_gpu(args):
     # kernels timed alone) are rated against the burst figure.
     in_loop, peak_regime = _peak_regime(ms_total, clocks, bf16_sust is not None,
                                         graph is not None)
+    alu_peak, alu_src = _alu_promotion_peak(torch, dev)
     fp8_loop_peak = (bf16_sust if in_loop else bf16_burst) * FP8_OVER_BF16
 
     crosscheck = None
@@ -1245,6 +1269,18 @@ def run_gpu(args):
                           "nominal_fp8_tflops": NOMINAL_FP8_TFLOPS,
                           "library_crosscheck": crosscheck}
                          if W.get("gemm_bound", "tensor") == "tensor" else
+                         {"bound": "alu", "achieved": gemm_tflops, "peak": alu_peak,
+                          "unit": "TFLOP/s", "frac": gemm_tflops / alu_peak,
+                          "traffic": _profile_traffic(*W["profile"]),
+                          "kernel": W["gemm_label"], "timing": timing,
+                          "peak_source": alu_src, "timed_region_ms": ms_total,
+                          "tensor_peak": fp8_peak,
+                          "frac_of_fp8_peak": gemm_tflops / fp8_peak,
+                          "frac_of_nominal_fp8": gemm_tflops / NOMINAL_FP8_TFLOPS,
+                          "achieved_isolated": tflops(g_iso),
+                          "frac_isolated": tflops(g_iso) / alu_peak,
+                          "frac_isolated_of_fp8_peak": tflops(g_iso) / fp8_peak}
+                         if W.get("gemm_bound") == "alu" else
                          {"bound": "hbm", "achieved": gemm_gbs, "peak": hbm, "unit": "GB/s",
                           "frac": gemm_gbs / hbm,
                           "traffic": _profile_traffic(*W["profile"]),

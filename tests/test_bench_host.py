@@ -81,3 +81,20 @@ def test_peak_regime():
     assert not bench._peak_regime(8.0, _c(["sw_power_cap"], sm=2060.0), True, False)[0]
     assert not bench._peak_regime(420.0, capped, True, True)[0]
     assert not bench._peak_regime(420.0, capped, False, False)[0]
+
+
+def test_alu_promotion_peak():
+    """The block-scaled GEMM's CUDA-core ceiling: 64 GEMM FLOP per FP32 FMA,
+    128 FMAs per SM per clock, every SM, the maximum SM clock."""
+    class Props:
+        multi_processor_count = 152
+
+    class FakeTorch:
+        class cuda:
+            @staticmethod
+            def get_device_properties(dev):
+                return Props()
+
+    peak, src = bench._alu_promotion_peak(FakeTorch, 0)
+    assert abs(peak - 64 * 128 * 152 * 2070e6 / 1e12) < 1e-6    # 2578.4 TFLOP/s
+    assert "128 FP32 FMA per SM per clock" in src and "152 SMs" in src
