@@ -46,6 +46,7 @@ GEMM_BYTES = 2 * N_SIZE * N_SIZE + 2 * N_SIZE * N_SIZE   # A, B codes + C bf16
 FP8_OVER_BF16 = 4.5 / 2.25        # nominal dense FP8 : BF16 tensor ratio
 NOMINAL_FP8_TFLOPS = 4500.0       # nominal dense FP8 tensor rate of one GB300
 SUSTAINED_MIN_MS = 2000.0         # timed regions this long are rated against the sustained peak
+NOMINAL_HBM_GBS = 8000.0          # GB300 HBM3e, nominal (~8 TB/s)
 POWER_CAPPED_CLOCK_FRAC = 0.95    # ... and so are those whose clocks sat below this under sw_power_cap
 WORKLOAD = ("per-tensor E4M3 quantize(A), quantize(B) + scaled GEMM, "
             "M=N=K=8192, A~N(0,1), B~N(0,0.02), 0.1% +-50sigma outliers, seed 0")
@@ -198,6 +199,23 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         return _summarise_clocks(self.rows, window)
+
+
+def _per_op(W, phases, alu_peak, fp8_peak):
+    """Each GEMM of a multi-GEMM step on its own: mean CUDA-event time of its
+    launches over the timed steps, TFLOP/s and fractions of the ALU and FP8
+    peaks (launches are recorded in step order, one per operation)."""
+    ops = W.get("per_op")
+    durs = (phases.get("launches") or {}).get("gemm") or []
+    if not ops or not durs or len(durs) % len(ops):
+        return None
+    out = {}
+    for i, (name, flops) in enumerate(ops):
+        ms = statistics.mean(durs[i::len(ops)])
+        tf = flops / (ms * 1e-3) / 1e12
+        out[name] = {"ms": ms, "tflops": tf, "frac": tf / alu_peak,
+                     "frac_of_fp8_peak": tf / fp8_peak}
+    return out
 
 
 def _alu_promotion_peak(torch, dev):
@@ -810,6 +828,7 @@ def _workload_blockscaled(fl, torch, dev, sptr, ph, linears=("qkv", "attn_out", 
             ph.mark("gemm")
 
     return dict(step=step, flops=flops, launches=12, quant_bytes_per_elem=5, gemm_bound="alu",
+                per_op=[(name, 2.0 * it[0] * it[1] * it[2]) for name, it in zip(linears, items)],
                 workload=("32x32 block-scaled E4M3: block-quantize activations [4096][K] ~ N(0,1) "
                           "and weights [N][K] ~ N(0,0.02), then the block-scaled GEMM, for the "
                           "four 70B-class linears qkv (10240,8192), attn_out (8192,8192), gate_up "
@@ -1279,7 +1298,8 @@ def run_gpu(args):
                           "frac_of_nominal_fp8": gemm_tflops / NOMINAL_FP8_TFLOPS,
                           "achieved_isolated": tflops(g_iso),
                           "frac_isolated": tflops(g_iso) / alu_peak,
-                          "frac_isolated_of_fp8_peak": tflops(g_iso) / fp8_peak}
+                          "frac_isolated_of_fp8_peak": tflops(g_iso) / fp8_peak,
+                          "per_op": _per_op(W, phases, alu_peak, fp8_peak)}
                          if W.get("gemm_bound") == "alu" else
                          {"bound": "hbm", "achieved": gemm_gbs, "peak": hbm, "unit": "GB/s",
                           "frac": gemm_gbs / hbm,
@@ -1294,6 +1314,9 @@ def run_gpu(args):
             "roofline_quantize": {"bound": "hbm", "achieved": quant_gbs, "peak": hbm,
                                   "unit": "GB/s",
                                   "frac": quant_gbs / hbm if quant_gbs else None,
+                                  "frac_of_nominal_hbm": (quant_gbs / NOMINAL_HBM_GBS
+                                                          if quant_gbs else None),
+                                  "nominal_hbm_gbs": NOMINAL_HBM_GBS,
                                   "traffic": (_profile_traffic(*W["qprofile"])
                                               if W.get("qprofile") else None),
                                   "algorithmic_bytes_per_elem": qbytes / W["quant_elems"], "timing": timing,

@@ -98,3 +98,13 @@ def test_alu_promotion_peak():
     peak, src = bench._alu_promotion_peak(FakeTorch, 0)
     assert abs(peak - 64 * 128 * 152 * 2070e6 / 1e12) < 1e-6    # 2578.4 TFLOP/s
     assert "128 FP32 FMA per SM per clock" in src and "152 SMs" in src
+
+
+def test_per_op_splits_launches_in_step_order():
+    W = {"per_op": [("a", 2e12), ("b", 4e12)]}
+    phases = {"launches": {"gemm": [1.0, 2.0, 3.0, 2.0]}}   # steps: (a 1, b 2), (a 3, b 2)
+    out = bench._per_op(W, phases, alu_peak=4000.0, fp8_peak=8000.0)
+    assert abs(out["a"]["ms"] - 2.0) < 1e-12 and abs(out["b"]["ms"] - 2.0) < 1e-12
+    assert abs(out["a"]["tflops"] - 1000.0) < 1e-9 and abs(out["b"]["tflops"] - 2000.0) < 1e-9
+    assert abs(out["b"]["frac"] - 0.5) < 1e-12 and abs(out["b"]["frac_of_fp8_peak"] - 0.25) < 1e-12
+    assert bench._per_op(W, {"launches": {"gemm": [1.0, 2.0, 3.0]}}, 1.0, 1.0) is None
