@@ -350,7 +350,7 @@ def run_reference(args):
                        "M": N_SIZE, "N": N_SIZE, "K": N_SIZE,
                        "l2": "inputs 2 x 268 MB fp32 > 129 MB L2; no flush"},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "cpu_model": _cpu_model(), "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -454,6 +454,24 @@ def _oracle_sample_workload(workload, linears=""):
     raise ValueError(workload)
 
 
+def _cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
+
+
 def _cpu_baseline_subprocess(flops, workload="pertensor8192", linears=""):
     """The oracle on the host cores, run in a child process so that its BLAS
     threads are set explicitly; about 10-30 s of CPU work on a sample of the
@@ -473,7 +491,7 @@ def _cpu_baseline_subprocess(flops, workload="pertensor8192", linears=""):
         return {"value": None, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                 "sample": "failed: %s" % exc}
     return {"value": flops / est / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "ms_per_step": est * 1e3,
+            "cpu_model": _cpu_model(), "ms_per_step": est * 1e3,
             "sample": "%s (%.1f s wall), scaled to one full step by element and output counts"
                       % (desc, wall)}
 
