@@ -68,6 +68,96 @@ def test_two_stream_pipeline_matches_serial():
     assert not torch.equal(ref[0], ref[1])
 
 
+def test_moe_two_stream_pipeline_matches_serial():
+    """The MoE step pipelined the same way: step i+1's grouped activation
+    quantisation and one-pass (carried-amax) weight quantisation on one
+    stream while step i's grouped GEMM runs on another, with the routing
+    offsets on the device.  Same results as the serial steps, bit for bit;
+    every step has new activations and new routing."""
+    import torch
+    fl = lib()
+    E, N, K, steps = 4, 256, 192, 5
+    rng = np.random.default_rng(31)
+    W = to_dev((rng.standard_normal((E, N, K)) * 0.02).astype(np.float32))
+    offs = []
+    Xs = []
+    for i in range(steps):
+        counts = rng.integers(0, 160, E) * (rng.random(E) > 0.2)
+        offs.append(to_dev(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)))
+        Xs.append(to_dev(rng.standard_normal((640, K)).astype(np.float32)))
+    P = lambda t, i=0: t.data_ptr() + i * t.element_size()
+
+    def quant(x, off, qx, ax, sx, qw, hist, parity, sw, s):
+        fl.fp8_quantize_pertensor_grouped(P(x), E, P(off), 640, K, K, P(qx), K, P(ax), P(sx), s)
+        for e in range(E):
+            fl.fp8_quantize_pertensor_delayed(P(W) + e * N * K * 4, N, K, K, P(qw) + e * N * K,
+                                              K, P(hist[parity ^ 1], e), P(hist[parity], e),
+                                              P(sw, e), 0, s)
+
+    def gemm(off, qx, sx, qw, sw, out, s):
+        fl.fp8_grouped_gemm(E, P(off), 640, P(qx), K, P(qw), K, N * K, P(out), N, N, K,
+                            P(sx), P(sw), s)
+
+    def seed_history():
+        hist = torch.empty((2, E), dtype=torch.float32, device="cuda")
+        sw = torch.empty(E, dtype=torch.float32, device="cuda")
+        q = torch.empty((E, N, K), dtype=torch.uint8, device="cuda")
+        for e in range(E):
+            for parity in (0, 1):
+                fl.fp8_quantize_pertensor(P(W) + e * N * K * 4, N, K, K, P(q) + e * N * K, K,
+                                          P(hist[parity], e), P(sw, e),
+                                          torch.cuda.current_stream().cuda_stream)
+        return hist
+
+    def buffers():
+        return (torch.empty((640, K), dtype=torch.uint8, device="cuda"),
+                torch.empty(E, dtype=torch.float32, device="cuda"),
+                torch.empty(E, dtype=torch.float32, device="cuda"),
+                torch.empty((E, N, K), dtype=torch.uint8, device="cuda"),
+                torch.empty(E, dtype=torch.float32, device="cuda"))
+
+    # serial reference
+    cur = torch.cuda.current_stream().cuda_stream
+    hist = seed_history()
+    qx, ax, sx, qw, sw = buffers()
+    ref = []
+    for i in range(steps):
+        out = torch.full((640, N), 9.0, dtype=torch.bfloat16, device="cuda")
+        quant(Xs[i], offs[i], qx, ax, sx, qw, hist, i & 1, sw, cur)
+        gemm(offs[i], qx, sx, qw, sw, out, cur)
+        ref.append(out)
+    torch.cuda.synchronize()
+
+    # pipelined
+    hist = seed_history()
+    bufs = [buffers(), buffers()]
+    outs = [torch.full((640, N), 9.0, dtype=torch.bfloat16, device="cuda") for _ in range(steps)]
+    main = torch.cuda.current_stream()
+    sq, sg = torch.cuda.Stream(), torch.cuda.Stream()
+    qdone = [torch.cuda.Event(), torch.cuda.Event()]
+    gdone = [torch.cuda.Event(), torch.cuda.Event()]
+    for ev in qdone + gdone:
+        ev.record(main)
+    sq.wait_stream(main)
+    sg.wait_stream(main)
+    for i in range(steps):
+        b = i & 1
+        qx, ax, sx, qw, sw = bufs[b]
+        sq.wait_event(gdone[b])
+        quant(Xs[i], offs[i], qx, ax, sx, qw, hist, i & 1, sw, sq.cuda_stream)
+        qdone[b].record(sq)
+        sg.wait_event(qdone[b])
+        gemm(offs[i], qx, sx, qw, sw, outs[i], sg.cuda_stream)
+        gdone[b].record(sg)
+    main.wait_stream(sq)
+    main.wait_stream(sg)
+    torch.cuda.synchronize()
+    assert fl.device_status() == 0
+    for i in range(steps):
+        assert torch.equal(outs[i].view(torch.int16), ref[i].view(torch.int16)), i
+    assert not torch.equal(ref[0], ref[1])
+
+
 def test_cuda_graph_capture_and_replay():
     """A quantize -> quantize -> GEMM step captured into a CUDA graph and
     replayed gives the eager result; replays see updated inputs."""
