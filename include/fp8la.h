@@ -184,7 +184,11 @@ FP8LA_API fp8la_status fp8_quantize_blockwise_32x32(const float *x, int64_t rows
  *   C[m][n] = bf16_rn( scale_a * scale_b * sum_k dec(A[m][k]) * dec(B[n][k]) )
  *
  * The sum is accumulated in FP32 on the tensor cores; the two scales are
- * applied once to the finished accumulator.  scale_a, scale_b: one fp32 each
+ * applied once to the finished accumulator, left to right as the scale
+ * paragraph writes it: fp32(fp32(acc * scale_a) * scale_b).  The scales are
+ * never multiplied together, so outputs inside the FP32 range stay exact to
+ * the bound even where scale_a * scale_b itself is not (two scales near
+ * 1e-23, or near 1e20).  scale_a, scale_b: one fp32 each
  * (device, read at run time, e.g. fp8_quantize_pertensor's scale_out).
  * Layout and alignment rules: see the file header.
  */
@@ -249,7 +253,12 @@ FP8LA_API fp8la_status fp8_quantize_pertensor_grouped(const float *x, int32_t nu
  *
  * Each 32-wide K block's partial sum is formed on the tensor cores and then
  * promoted, multiplied by its tile-scale product, into an FP32 accumulator
- * on the CUDA cores.  sa: fp32 [ceil(M/32)][ld_sa], ld_sa >= ceil(K/32);
+ * on the CUDA cores.  The tile-scale product sa * sb is formed in FP32 (once
+ * per pair of tiles, not per output), so the results meet the bound while
+ * every product is a normal FP32 number; for scales amax / 448 from
+ * fp8_quantize_blockwise_32x32 that is two tiles whose amax values multiply
+ * to between 448^2 2^-126 (about 2.4e-33) and 448^2 2^128 (about 6.8e43).
+ * sa: fp32 [ceil(M/32)][ld_sa], ld_sa >= ceil(K/32);
  * sb: fp32 [ceil(N/32)][ld_sb], ld_sb >= ceil(K/32).  All device.  The
  * scale grids are read by TMA: sa and sb must be 16-byte aligned and ld_sa,
  * ld_sb multiples of 4 (otherwise FP8LA_ERR_ALIGNMENT).
@@ -280,7 +289,7 @@ FP8LA_API fp8la_status fp8_gemm_blockscaled_32x32(const uint8_t *A, int64_t lda,
  * rows at or past m_offsets[num_groups] are neither read for any output nor
  * written.
  * Groups with no rows are skipped.  scale_a, scale_b: fp32 [num_groups]
- * (device).  b_group_stride (elements) must be a multiple of 16 and
+ * (device), applied as in fp8_gemm.  b_group_stride (elements) must be a multiple of 16 and
  * >= N * ldb.  1 <= num_groups <= 1024.
  */
 FP8LA_API fp8la_status fp8_grouped_gemm(int32_t num_groups, const int32_t *m_offsets,

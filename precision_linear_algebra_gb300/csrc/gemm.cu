@@ -26,8 +26,9 @@
 //     epilogue of tile i overlaps the MMAs of tile i+1.
 //   * warps 0-3: epilogue.  Warp w owns TMEM lanes (= C rows) 32w..32w+31;
 //     each thread loads its row's accumulator 32 columns at a time
-//     (tcgen05.ld), multiplies by scale_a*scale_b, rounds to BF16 and writes
-//     16-byte vectors; then releases the accumulator (`tmem_empty`).
+//     (tcgen05.ld), multiplies by scale_a and then by scale_b, rounds to
+//     BF16 and writes 16-byte vectors; then releases the accumulator
+//     (`tmem_empty`).
 //   * Tiles are visited in a grouped order (GROUP_M row blocks per group)
 //     so that concurrently running CTAs share A and B tiles through L2.
 //   * Ragged M, N, K: TMA fills out-of-range operand elements with zeros;
@@ -189,12 +190,21 @@ __device__ __forceinline__ void load_group_offsets(const GemmArgs &a,
   }
 }
 
-// Epilogue of one accumulator row: 32 FP32 columns of TMEM -> x scale ->
+// acc * scale_a * scale_b, evaluated left to right as the scale paragraph
+// writes it: (acc * scale_a) * scale_b.  The two scales are never multiplied
+// together, so a product of scales outside the FP32 range (two tiny scales,
+// or two huge ones) does not flush or overflow an output that is itself in
+// range, and a zero accumulator stays zero.  scale = {scale_a, scale_b}.
+__device__ __forceinline__ float apply_scales(uint32_t acc, float2 scale) {
+  return __fmul_rn(__fmul_rn(__uint_as_float(acc), scale.x), scale.y);
+}
+
+// Epilogue of one accumulator row: 32 FP32 columns of TMEM -> x scales ->
 // BF16 (round to nearest even) -> C[row][n .. n+31], clipped at N.  Every
 // lane of the warp must call it (tcgen05.ld is warp-collective).
 __device__ __forceinline__ void store_chunk32(uint32_t taddr, bool row_ok,
                                               uint16_t *crow, int n, int N,
-                                              float scale, bool vec16) {
+                                              float2 scale, bool vec16) {
   uint32_t v[32];
   tmem_ld32(taddr, v);
   if (!row_ok || n >= N) return;
@@ -202,8 +212,8 @@ __device__ __forceinline__ void store_chunk32(uint32_t taddr, bool row_ok,
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const __nv_bfloat162 h =
-        __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * j]), scale),
-                              __fmul_rn(__uint_as_float(v[2 * j + 1]), scale));
+        __floats2bfloat162_rn(apply_scales(v[2 * j], scale),
+                              apply_scales(v[2 * j + 1], scale));
     w[j] = *reinterpret_cast<const uint32_t *>(&h);
   }
   if (vec16 && n + 32 <= N) {
@@ -227,7 +237,7 @@ __device__ __forceinline__ void store_chunk32(uint32_t taddr, bool row_ok,
 // consecutive BF16 of one C row.  Every lane of the warp must call it.
 __device__ __forceinline__ void store_chunk32_t(uint32_t taddr, uint16_t *C,
                                                 int64_t ldc, int m0, int m_end,
-                                                int n, int N, float scale) {
+                                                int n, int N, float2 scale) {
   uint32_t v[32];
   tmem_ld32(taddr, v);
   if (n >= N) return;
@@ -236,7 +246,7 @@ __device__ __forceinline__ void store_chunk32_t(uint32_t taddr, uint16_t *C,
   for (int j = 0; j < 32; ++j)
     if (m0 + j < m_end) {
       const __nv_bfloat16 h =
-          __float2bfloat16_rn(__fmul_rn(__uint_as_float(v[j]), scale));
+          __float2bfloat16_rn(apply_scales(v[j], scale));
       cp[static_cast<int64_t>(j) * ldc] = *reinterpret_cast<const uint16_t *>(&h);
     }
 }
@@ -253,15 +263,15 @@ __device__ __forceinline__ void store_chunk32_tma(uint32_t taddr,
                                                   uint32_t stage, int lane,
                                                   const CUtensorMap *tmC,
                                                   int n, int row0,
-                                                  float scale) {
+                                                  float2 scale) {
   uint32_t v[32];
   tmem_ld32(taddr, v);
   uint32_t w[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const __nv_bfloat162 h =
-        __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * j]), scale),
-                              __fmul_rn(__uint_as_float(v[2 * j + 1]), scale));
+        __floats2bfloat162_rn(apply_scales(v[2 * j], scale),
+                              apply_scales(v[2 * j + 1], scale));
     w[j] = *reinterpret_cast<const uint32_t *>(&h);
   }
   if (lane == 0) bulk_wait_read_all();
@@ -434,13 +444,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     uint32_t local = 0;
-    float scale = 1.0f;
+    float2 scale = make_float2(1.0f, 1.0f);
     int cur_group = -1;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++local) {
       const TileInfo ti =
           tile_info<GROUPED, BM>(t, a, tiles_n, pref, offs_smem, BN);
       if (ti.group != cur_group) {
-        scale = __fmul_rn(a.scale_a[ti.group], a.scale_b[ti.group]);
+        scale = make_float2(a.scale_a[ti.group], a.scale_b[ti.group]);
         cur_group = ti.group;
       }
       const uint32_t buf = local & 1u, use = local >> 1;
@@ -755,7 +765,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   } else {
     // ----------------------------------------------- epilogue (both CTAs)
     uint32_t local = 0;
-    float scale = 1.0f;
+    float2 scale = make_float2(1.0f, 1.0f);
     int cur_group = -1;
     const uint32_t leader_tempty0 = mapa_shared(tempty_bar(0), lrank);
     const uint32_t leader_tempty1 = mapa_shared(tempty_bar(1), lrank);
@@ -770,7 +780,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       const int width = (half < 0 ? P_BN : P_BN / 2) / 2;   // this warp's share
       const int col0 = col_half * width;
       if (ti.group != cur_group) {
-        scale = __fmul_rn(a.scale_a[ti.group], a.scale_b[ti.group]);
+        scale = make_float2(a.scale_a[ti.group], a.scale_b[ti.group]);
         cur_group = ti.group;
       }
       const uint32_t buf = local & 1u, use = local >> 1;
