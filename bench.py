@@ -895,20 +895,20 @@ def _workload_grouped(fl, torch, dev, sptr, ph):
                                       P(hist_w[parity], e), P(sw, e), sptr)
     counter = [0]
 
-    def quant(b, s):
+    def quant(b, s, Xd=X, Wd=W):
         parity = counter[0] & 1
         counter[0] += 1
         # every expert's activation rows in one call, the offsets read on
         # the device (as the grouped GEMM reads them)
-        fl.fp8_quantize_pertensor_grouped(P(X), E, d_off.data_ptr(), Mt, K, K, P(qx2[b]), K,
+        fl.fp8_quantize_pertensor_grouped(P(Xd), E, d_off.data_ptr(), Mt, K, K, P(qx2[b]), K,
                                           P(amax2[b]), P(sx2[b]), s)
         for e in range(E):
             fl.fp8_quantize_pertensor_delayed(
-                P(W) + e * N * K * 4, N, K, K, P(qw2[b]) + e * N * K, K,
+                P(Wd) + e * N * K * 4, N, K, K, P(qw2[b]) + e * N * K, K,
                 P(hist_w[parity ^ 1], e), P(hist_w[parity], e), P(sw2[b], e), 0, s)
 
-    def gemm(b, s):
-        fl.fp8_grouped_gemm(E, d_off.data_ptr(), Mt, P(qx2[b]), K, P(qw2[b]), K, N * K, P(C),
+    def gemm(b, s, Cd=C):
+        fl.fp8_grouped_gemm(E, d_off.data_ptr(), Mt, P(qx2[b]), K, P(qw2[b]), K, N * K, P(Cd),
                             N, N, K, P(sx2[b]), P(sw2[b]), s)
 
     def step():
@@ -951,7 +951,65 @@ def _workload_grouped(fl, torch, dev, sptr, ph):
         main.wait_stream(sq)
         main.wait_stream(sg)
 
-    return dict(step=step, pipeline=(pbegin, pstep, pend), flops=2.0 * Mt * N * K,
+    # Pipelined end to end, as for the 8192^3 workload: step i's activations
+    # and weights come from pinned host memory on two copy streams, its C
+    # goes back on a third; the host->device copies of step i+1, compute of
+    # step i and the device->host copy of step i-1 overlap (the link carries
+    # both directions at once).  Device inputs and C are double-buffered.
+    e2e = {}
+
+    def ebegin(X_h, W_h, C_h2):
+        if not e2e:
+            e2e.update(X=[X, torch.empty_like(X)], W=[W, torch.empty_like(W)],
+                       C=[C, torch.empty_like(C)],
+                       sx=torch.cuda.Stream(dev), sw=torch.cuda.Stream(dev),
+                       so=torch.cuda.Stream(dev),
+                       quantized=[torch.cuda.Event(), torch.cuda.Event()],
+                       computed=[torch.cuda.Event(), torch.cuda.Event()],
+                       stored=[torch.cuda.Event(), torch.cuda.Event()])
+        e2e.update(X_h=X_h, W_h=W_h, C_h=C_h2)
+        for k in ("quantized", "computed", "stored"):
+            for ev in e2e[k]:
+                ev.record(main)
+        for st in (e2e["sx"], e2e["sw"], e2e["so"], sq, sg):
+            st.wait_stream(main)
+
+    def estep(i):
+        b = i & 1
+        T = e2e
+        # inputs: buffer b is free once quantize(i-2) has read it
+        T["sx"].wait_event(T["quantized"][b])
+        T["sw"].wait_event(T["quantized"][b])
+        with torch.cuda.stream(T["sx"]):
+            T["X"][b].copy_(T["X_h"], non_blocking=True)
+        with torch.cuda.stream(T["sw"]):
+            T["W"][b].copy_(T["W_h"], non_blocking=True)
+        ev_x, ev_w = torch.cuda.Event(), torch.cuda.Event()
+        ev_x.record(T["sx"])
+        ev_w.record(T["sw"])
+        sq.wait_event(ev_x)
+        sq.wait_event(ev_w)
+        sq.wait_event(gdone[b])
+        quant(b, sq.cuda_stream, T["X"][b], T["W"][b])
+        T["quantized"][b].record(sq)
+        qdone[b].record(sq)
+        # GEMM into C[b] once the device->host copy of step i-2 has read it
+        sg.wait_event(qdone[b])
+        sg.wait_event(T["stored"][b])
+        gemm(b, sg.cuda_stream, T["C"][b])
+        gdone[b].record(sg)
+        T["computed"][b].record(sg)
+        T["so"].wait_event(T["computed"][b])
+        with torch.cuda.stream(T["so"]):
+            T["C_h"][b].copy_(T["C"][b], non_blocking=True)
+        T["stored"][b].record(T["so"])
+
+    def eend():
+        for st in (e2e["sx"], e2e["sw"], e2e["so"], sq, sg):
+            main.wait_stream(st)
+
+    return dict(step=step, pipeline=(pbegin, pstep, pend), e2e_pipeline=(ebegin, estep, eend),
+                flops=2.0 * Mt * N * K,
                 launches=2 + E + 1,
                 workload=("grouped MoE E4M3: 8 experts, K 4096, N 14336, 8192 tokens top-2 "
                           "(16384 rows, Dirichlet(1) counts %s), per-expert per-tensor quantize "
@@ -1219,6 +1277,16 @@ def run_gpu(args):
             e2e_runs.append(e0.elapsed_time(e1) / e2e_steps)
     else:
         e2e_runs = [time_serial() for _ in range(E2E_REPEATS)]
+    e2e_equal = None
+    if e2e_pipelined:
+        # The host copy of the last pipelined step's output against the
+        # device output of a plain step on the same inputs, bit for bit.
+        last = C_h2[(e2e_steps - 1) & 1]
+        step()
+        torch.cuda.synchronize()
+        dev_out = outs[0][0].cpu()
+        e2e_equal = bool(torch.equal(last.view(torch.int16), dev_out.view(torch.int16)))
+        del dev_out
     e2e_ms = statistics.median(e2e_runs)
     e2e_serial_ms = statistics.median(e2e_serial_runs) if e2e_serial_runs else None
     if world > 1:
@@ -1357,7 +1425,8 @@ def run_gpu(args):
                     "schedule": "pipelined" if e2e_pipelined else "serial",
                     "serial_ms_per_step": e2e_serial_ms if e2e_pipelined else e2e_ms,
                     "runs_ms_per_step": e2e_runs,
-                    "serial_runs_ms_per_step": e2e_serial_runs or e2e_runs},
+                    "serial_runs_ms_per_step": e2e_serial_runs or e2e_runs,
+                    "pipelined_output_equals_device": e2e_equal},
             "gpu_launches": W["launches"] * args.steps * (len(args.linears.split(",")) / 4.0
                                                            if args.workload == "blockscaled"
                                                            and args.linears else 1),
