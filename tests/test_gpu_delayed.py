@@ -101,3 +101,21 @@ def test_empty_and_aliasing():
     st = fl.load().fp8_quantize_pertensor_delayed(P(x), 1, 4, 4, P(q), 4, P(words, 0),
                                                   P(words, 0), P(words, 2), 0, s)
     assert st == fl.FP8LA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_special_carried_amax_and_inputs(fmt):
+    """Degenerate carried-over amax values (+Inf: qscale 0; NaN and fp32
+    subnormals: qscale not finite, so qscale = scale = 1; the fp32 maximum)
+    and inputs holding +-Inf, NaN, signed zeros and subnormals, whose
+    recorded amax ignores the NaN and is Inf."""
+    fl = lib()
+    rng = np.random.default_rng(19)
+    x = (rng.standard_normal((37, 90)) * 5).astype(np.float32)
+    x[0, :6] = [np.inf, -np.inf, np.nan, 0.0, -0.0, 1e-42]
+    x[36, 89] = np.nan
+    clean = x.copy()
+    clean[0, :3] = [1.0, -2.0, 3.0]
+    for xx in (x, clean):
+        for prev in (np.inf, np.nan, 1e-40, 3.4e38, 448.0):
+            _check(_run(fl, xx, prev, fmt, 3, 8), xx, prev, fmt)

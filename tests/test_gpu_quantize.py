@@ -166,3 +166,56 @@ def test_blockwise_transformer_weights_sampled():
         rq, rs = oracle.quantize_blockwise_32x32(W[r0:r0 + 64, c0:c0 + 64])
         assert np.array_equal(qn[r0:r0 + 64, c0:c0 + 64], rq)
         assert np.array_equal(sn[r0 // 32:r0 // 32 + 2, c0 // 32:c0 // 32 + 2], rs)
+
+
+def _special_tiles():
+    """A [101][136] fp32 array whose 32 x 32 tiles hold the degenerate cases
+    of the per-tile scale rule: all zeros, signed zeros, +Inf and -Inf (amax
+    Inf: qscale 0, scale Inf), NaN (ignored by the amax, coded 0x7F), fp32
+    subnormals only (448/amax overflows: qscale = scale = 1), values near the
+    fp32 maximum, values that land exactly on 448 and on E4M3 rounding
+    midpoints; the last tile row and column are ragged."""
+    rng = np.random.default_rng(77)
+    x = (rng.standard_normal((101, 136)) * 3).astype(np.float32)
+    t = lambda i, j: (slice(32 * i, 32 * i + 32), slice(32 * j, 32 * j + 32))
+    x[t(0, 0)] = 0.0
+    x[t(0, 1)] = -0.0
+    x[t(0, 1)][5, 7] = 0.0
+    x[t(0, 2)][3, 3] = np.inf
+    x[t(0, 3)][31, 0] = -np.inf
+    x[t(0, 3)][0, 31] = np.nan
+    x[t(1, 0)][:, :] = np.nan
+    x[t(1, 0)][4, 4] = 2.5
+    x[t(1, 1)] = rng.standard_normal((32, 32)).astype(np.float32) * np.float32(1e-40)
+    x[t(1, 2)] = (rng.uniform(-3.0, 3.0, (32, 32)) * 1e38).astype(np.float32)
+    x[t(1, 2)][0, 0] = np.float32(3.4e38)
+    # amax 448: the codes are the values themselves, including midpoints
+    # between E4M3 neighbours (ties to even)
+    mids = np.array([448.0, -448.0, 1.0625, 1.1875, 17.0, 19.0, 0.001953125 * 1.5,
+                     240.0, 232.0, 0.5], np.float32)
+    x[t(1, 3)] = 0.25
+    x[t(1, 3)][0, :mids.size] = mids
+    x[t(2, 4)][0, 0] = np.inf            # ragged corner tile (rows 96..100, cols 128..135)
+    return x
+
+
+def test_blockwise_special_tiles():
+    import torch
+    fl = lib()
+    x = _special_tiles()
+    xs = torch.zeros((x.shape[0], x.shape[1] + 4), dtype=torch.float32, device="cuda")
+    xs[:, :x.shape[1]] = to_dev(x)
+    for view in (xs[:, :x.shape[1]], to_dev(x)):      # padded stride, then contiguous
+        q, s = fl.quantize_blockwise_32x32(view)
+        torch.cuda.synchronize()
+        assert fl.device_status() == 0
+        rq, rs = oracle.quantize_blockwise_32x32(x)
+        got_q = q.cpu().numpy()
+        diff = np.argwhere(got_q != rq)
+        assert diff.size == 0, "codes differ at %d places, first %s: got %#x want %#x" % (
+            len(diff), tuple(diff[0]), got_q[tuple(diff[0])], rq[tuple(diff[0])])
+        assert np.array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    # the cases the array is meant to hold
+    assert rs[0, 0] == 1.0 and rs[0, 2] == np.inf and rs[1, 1] == 1.0 and rs[1, 3] == 1.0
+    assert np.isfinite(rs[1, 2]) and rs[2, 4] == np.inf
+    assert np.all(rq[32:64, 0:32][np.isnan(x[32:64, 0:32])] == 0x7F)

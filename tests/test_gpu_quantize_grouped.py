@@ -91,3 +91,31 @@ def test_bad_offsets_write_nothing_and_are_reported(offs):
     assert status == fl.FP8LA_ERR_DEVICE_ARG
     assert np.all(qs == SENTINEL), "codes written for bad offsets"
     assert np.all(scale == -1.0), "scales written for bad offsets"
+
+
+def test_special_value_groups():
+    """Groups holding the degenerate cases of the scale rule: zeros, signed
+    zeros, +Inf (amax Inf: qscale 0, scale Inf), NaN beside finite values,
+    NaN only (amax 0), fp32 subnormals only (448/amax overflows: qscale =
+    scale = 1), values near the fp32 maximum, and an ordinary group."""
+    fl = lib()
+    rng = np.random.default_rng(31)
+    cols = 72
+    parts = [np.zeros((5, cols), np.float32),
+             np.full((3, cols), -0.0, np.float32),
+             rng.standard_normal((9, cols)).astype(np.float32),
+             rng.standard_normal((4, cols)).astype(np.float32),
+             np.full((2, cols), np.nan, np.float32),
+             (rng.standard_normal((6, cols)) * 1e-40).astype(np.float32),
+             (rng.uniform(-3.0, 3.0, (7, cols)) * 1e38).astype(np.float32),
+             (rng.standard_normal((11, cols)) * 0.02).astype(np.float32)]
+    parts[2][4, 5] = np.inf
+    parts[3][1, :3] = np.nan
+    parts[6][0, 0] = np.float32(3.4e38)
+    x = np.concatenate(parts)
+    offs = np.concatenate([[0], np.cumsum([p.shape[0] for p in parts])]).astype(np.int32)
+    got = _run(fl, x, offs, cap_extra=6, ldx_pad=4, ldq_pad=8)
+    _check(got, x, offs, cols)
+    _, amax, scale, _ = got
+    assert amax[0] == 0 and scale[0] == 1 and scale[2] == np.inf and amax[4] == 0
+    assert scale[5] == 1 and np.isfinite(scale[6])
