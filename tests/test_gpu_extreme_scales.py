@@ -148,3 +148,36 @@ def test_blockscaled_gemm_small_normal_scale_products():
     assert_within_bound(got, r, oracle.tolerance_blockscaled_32x32(A, B, sa, sb, r),
                         "block-scaled, small tile-scale products")
     assert np.all(got[7] == 0)
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2])
+@pytest.mark.parametrize("sa,sb", [(np.inf, 0.5), (1.0, -np.inf), (np.nan, 1.0), (0.0, 3.0),
+                                   (np.inf, 0.0)])
+def test_pertensor_gemm_nonfinite_and_zero_scales(sa, sb, variant):
+    """A tensor holding +-Inf gets scale Inf from the quantiser.  With a
+    non-finite or zero scale every output follows IEEE arithmetic on the
+    exact product: +-Inf where the sum is nonzero, NaN where an infinite scale
+    meets a zero sum (or a NaN scale), zero for a zero scale.  The GPU must
+    give the oracle's value class and sign at every output."""
+    import torch
+    fl = lib()
+    rng = np.random.default_rng(90 + variant)
+    M, N, K = 200, 144, 64
+    A, B = random_codes(rng, (M, K)), random_codes(rng, (N, K))
+    A[9] = 0                      # zero sums in row 9
+    sa, sb = np.float32(sa), np.float32(sb)
+    fl.fp8la_set_gemm_variant(variant)
+    try:
+        C = fl.gemm(to_dev(A), to_dev(B), torch.tensor([sa], device="cuda"),
+                    torch.tensor([sb], device="cuda"))
+        torch.cuda.synchronize()
+    finally:
+        fl.fp8la_set_gemm_variant(0)
+    assert fl.device_status() == 0
+    with np.errstate(invalid="ignore"):
+        r, _ = oracle.gemm_pertensor(A, B, sa, sb)
+    got = bf16_to_f64(C)
+    assert np.array_equal(np.isnan(got), np.isnan(r))
+    fin = ~np.isnan(r)
+    assert np.all(np.isinf(r[fin]) | (r[fin] == 0)), "the case has other outputs"
+    assert np.array_equal(got[fin], r[fin])      # +-Inf with the oracle's sign, or 0
