@@ -242,3 +242,50 @@ def test_tail_tiles_of_every_size(N, K, variant):
         if hi > lo:
             check_pertensor(got[lo:hi], A[lo:hi], B[e], sa[e], sb[e], what="group %d" % e)
     assert np.all(got[offs[-1]:] == 3.0), "rows past the last group were written"
+
+
+def test_maximum_group_count(variant):
+    """num_groups = 1024, the largest the header allows: most groups empty,
+    some of one to a few rows, a few spanning several row tiles, the last
+    groups empty; each expert's own scales; every nonempty group against the
+    oracle and rows past the last group untouched."""
+    fl = lib()
+    rng = np.random.default_rng(1024)
+    E, N, K = 1024, 96, 64
+    counts = np.zeros(E, np.int64)
+    small = rng.choice(E - 8, 60, replace=False)
+    counts[small] = rng.integers(1, 5, 60)
+    counts[[3, 500, 1000]] = [130, 257, 31]
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    A = random_codes(rng, (int(offs[-1]), K))
+    B = random_codes(rng, (E, N, K))
+    sa = rng.uniform(0.01, 2, E).astype(np.float32)
+    sb = rng.uniform(0.01, 2, E).astype(np.float32)
+    got = _grouped(fl, A, offs, B, sa, sb, cap_extra=21)
+    for e in np.flatnonzero(counts):
+        lo, hi = offs[e], offs[e + 1]
+        check_pertensor(got[lo:hi], A[lo:hi], B[e], sa[e], sb[e], what="group %d" % e)
+    assert np.all(got[offs[-1]:] == 3.0), "rows past the last group were written"
+
+
+def test_k_zero_writes_zeros_in_groups_only():
+    """K = 0: every row inside a group becomes zero, with the offsets read on
+    the device; rows past the last group keep their sentinel."""
+    import torch
+    fl = lib()
+    counts = [5, 0, 130, 1]
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    E, N, cap = len(counts), 72, 160
+    dC = torch.full((cap, N), 3.0, dtype=torch.bfloat16, device="cuda")
+    dA = torch.zeros((cap, 16), dtype=torch.uint8, device="cuda")
+    dB = torch.zeros((E, N, 16), dtype=torch.uint8, device="cuda")
+    ones = torch.ones(E, dtype=torch.float32, device="cuda")
+    d_off = to_dev(offs)
+    fl.fp8_grouped_gemm(E, d_off.data_ptr(), cap, dA.data_ptr(), 16, dB.data_ptr(), 16,
+                        N * 16, dC.data_ptr(), N, N, 0, ones.data_ptr(), ones.data_ptr(),
+                        torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert fl.device_status() == 0
+    got = bf16_to_f64(dC)
+    assert np.all(got[:offs[-1]] == 0)
+    assert np.all(got[offs[-1]:] == 3.0)

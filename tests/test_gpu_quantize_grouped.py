@@ -119,3 +119,18 @@ def test_special_value_groups():
     _, amax, scale, _ = got
     assert amax[0] == 0 and scale[0] == 1 and scale[2] == np.inf and amax[4] == 0
     assert scale[5] == 1 and np.isfinite(scale[6])
+
+
+def test_maximum_group_count():
+    """1024 groups, the largest the header allows, most of them empty."""
+    fl = lib()
+    rng = np.random.default_rng(4096)
+    E, cols = 1024, 40
+    counts = np.zeros(E, np.int64)
+    idx = rng.choice(E, 80, replace=False)
+    counts[idx] = rng.integers(1, 9, 80)
+    counts[777] = 300
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    x = (rng.standard_normal((int(offs[-1]), cols))
+         * 10.0 ** rng.uniform(-3, 3, (int(offs[-1]), 1))).astype(np.float32)
+    _check(_run(fl, x, offs, cap_extra=9, ldx_pad=4, ldq_pad=8), x, offs, cols)
