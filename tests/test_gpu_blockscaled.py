@@ -193,3 +193,19 @@ def test_transformer_linears_full_size_sampled(name):
         rows = np.arange(i0, min(M, i0 + 1024))
         check_block(Cg[i0:i0 + rows.size], A, B, sa, sb, rows=rows,
                     cols=np.arange(c0, c0 + 64), what="%s cols %d.." % (name, c0), maxes=maxes)
+
+
+def test_long_k_all_outputs():
+    """K = 65530: 512 stages per tile (the 7-slot ring wraps 73 times), 2048
+    scale blocks along K with a ragged last one; every output within the
+    bound."""
+    fl = lib()
+    rng = np.random.default_rng(65530)
+    M, N, K = 160, 200, 65530
+    A, B = random_codes(rng, (M, K)), random_codes(rng, (N, K))
+    nkb = -(-K // 32)
+    sa = rng.uniform(1e-3, 2.0, (-(-M // 32), nkb)).astype(np.float32)
+    sb = rng.uniform(1e-3, 2.0, (-(-N // 32), nkb)).astype(np.float32)
+    got = _run(fl, A, B, sa, sb)
+    frac = check_block(got, A, B, sa, sb, what="K %d" % K)
+    assert frac > 0.9

@@ -164,3 +164,25 @@ def test_8192_outliers_sampled(variant):
     cols = np.sort(rng.choice(8192, 64, replace=False))
     check_pertensor(Cn[rows], rqa, rqb, rsa, rsb, rows=rows, what="rows")
     check_pertensor(Cn[:, cols], rqa, rqb, rsa, rsb, cols=cols, what="cols")
+
+
+@pytest.mark.parametrize("M,N,K,positive", [
+    (300, 280, 131071, False),   # the longest K whose oracle sum is exact; ragged
+    (256, 256, 65536, True),     # all-positive codes: no cancellation, the
+                                 # FP32 accumulation error is largest relative
+                                 # to the sum
+])
+def test_long_k_all_outputs(M, N, K, positive, variant):
+    """Long reductions: about a thousand 128-wide K stages per tile, so the
+    stage ring wraps hundreds of times; every output within the bound."""
+    fl = lib()
+    rng = np.random.default_rng(K + M)
+    if positive:
+        codes = np.arange(0x08, 0x7F, dtype=np.uint8)       # positive normals
+        A, B = rng.choice(codes, (M, K)), rng.choice(codes, (N, K))
+    else:
+        A, B = random_codes(rng, (M, K)), random_codes(rng, (N, K))
+    sa, sb = np.float32(0.0123), np.float32(0.731)
+    got = _gemm(fl, A, B, sa, sb)
+    frac = check_pertensor(got, A, B, sa, sb, what="K %d" % K)
+    assert frac > 0.9

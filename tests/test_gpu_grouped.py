@@ -289,3 +289,22 @@ def test_k_zero_writes_zeros_in_groups_only():
     got = bf16_to_f64(dC)
     assert np.all(got[:offs[-1]] == 0)
     assert np.all(got[offs[-1]:] == 3.0)
+
+
+def test_long_k(variant):
+    """K = 65536 over three groups (one empty): hundreds of laps of the
+    stage ring per tile, every output within the bound."""
+    fl = lib()
+    rng = np.random.default_rng(65536)
+    counts = [150, 0, 70]
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    E, N, K = len(counts), 136, 65536
+    A = random_codes(rng, (int(offs[-1]), K))
+    B = random_codes(rng, (E, N, K))
+    sa = rng.uniform(0.01, 2, E).astype(np.float32)
+    sb = rng.uniform(0.01, 2, E).astype(np.float32)
+    got = _grouped(fl, A, offs, B, sa, sb, cap_extra=10)
+    for e in (0, 2):
+        lo, hi = offs[e], offs[e + 1]
+        check_pertensor(got[lo:hi], A[lo:hi], B[e], sa[e], sb[e], what="group %d" % e)
+    assert np.all(got[offs[-1]:] == 3.0)
