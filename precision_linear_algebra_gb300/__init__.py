@@ -200,6 +200,14 @@ def _ld(t):
     return t.stride(0) if t.shape[0] > 1 else max(t.shape[1], 1)
 
 
+def _ld_tma(t):
+    """As _ld, for an FP8 GEMM operand, whose row stride goes into a TMA
+    descriptor (a multiple of 16 bytes even when there is one row: the
+    stride of a single row never addresses memory, so the row length
+    rounded up to 16 is passed)."""
+    return t.stride(0) if t.shape[0] > 1 else (max(t.shape[1], 1) + 15) // 16 * 16
+
+
 def _ld_scales(t):
     """As _ld, for a block-scale grid, whose row stride the GEMM reads by TMA
     (a multiple of 4 floats even when there is one row)."""
@@ -294,10 +302,10 @@ def gemm(A, B, scale_a, scale_b, C=None, a_fmt="e4m3", b_fmt="e4m3"):
     if C is None:
         C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     if a_fmt == "e4m3" and b_fmt == "e4m3":
-        fp8_gemm(_ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C),
+        fp8_gemm(_ptr(A), _ld_tma(A), _ptr(B), _ld_tma(B), _ptr(C), _ld(C),
                  M, N, K, _ptr(scale_a), _ptr(scale_b), _stream())
     else:
-        fp8_gemm_ex(_ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C),
+        fp8_gemm_ex(_ptr(A), _ld_tma(A), _ptr(B), _ld_tma(B), _ptr(C), _ld(C),
                     M, N, K, _ptr(scale_a), _ptr(scale_b), _FORMATS[a_fmt],
                     _FORMATS[b_fmt], _stream())
     return C
@@ -310,7 +318,7 @@ def gemm_blockscaled_32x32(A, B, sa, sb, C=None):
     N = B.shape[0]
     if C is None:
         C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
-    fp8_gemm_blockscaled_32x32(_ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C),
+    fp8_gemm_blockscaled_32x32(_ptr(A), _ld_tma(A), _ptr(B), _ld_tma(B), _ptr(C),
                                _ld(C), M, N, K, _ptr(sa), _ld_scales(sa),
                                _ptr(sb), _ld_scales(sb), _stream())
     return C
@@ -324,8 +332,10 @@ def grouped_gemm(m_offsets, A, B, scale_a, scale_b, C=None):
     N = B.shape[1]
     if C is None:
         C = torch.empty((cap, N), dtype=torch.bfloat16, device=A.device)
-    fp8_grouped_gemm(E, _ptr(m_offsets), cap, _ptr(A), _ld(A), _ptr(B),
-                     B.stride(1) if N > 1 else K, B.stride(0), _ptr(C), _ld(C), N, K,
+    ldb = B.stride(1) if N > 1 else (max(K, 1) + 15) // 16 * 16
+    bstride = B.stride(0) if E > 1 else N * ldb
+    fp8_grouped_gemm(E, _ptr(m_offsets), cap, _ptr(A), _ld_tma(A), _ptr(B),
+                     ldb, bstride, _ptr(C), _ld(C), N, K,
                      _ptr(scale_a), _ptr(scale_b), _stream())
     return C
 

@@ -9,7 +9,11 @@ Guard columns past N and guard rows past M (past the last group for the
 grouped GEMM) must come back untouched.  The quantisers run on random ragged
 shapes with padded row strides and must match the oracle bit for bit.
 Shapes, codes and scales come from fixed seeds, so a failure reproduces.
+FP8LA_FUZZ_MULT=n runs n times as many cases of each kind; the first ones
+are the default run's.
 """
+
+import os
 
 import numpy as np
 import pytest
@@ -18,6 +22,8 @@ import oracle
 from _helpers import assert_within_bound, bf16_to_f64, lib, random_codes, to_dev
 
 pytestmark = pytest.mark.gpu
+
+_MULT = max(1, int(os.environ.get("FP8LA_FUZZ_MULT", "1")))
 
 SENTINEL = -7.0
 
@@ -54,11 +60,11 @@ def _guards_untouched(full, rows, N):
     return np.all(f[rows:, :] == SENTINEL) and np.all(f[:, N:] == SENTINEL)
 
 
-@pytest.mark.parametrize("case", range(40))
+@pytest.mark.parametrize("case", range(40 * _MULT))
 def test_pertensor_gemm_random_shapes(case):
     import torch
     fl = lib()
-    M, N, K = _shapes(101, 40)[case]
+    M, N, K = _shapes(101, 40 * _MULT)[case]
     variant = [0, 1, 2, 3, 4][case % 5]
     rng = np.random.default_rng(1000 + case)
     A, B = random_codes(rng, (M, K)), random_codes(rng, (N, K))
@@ -80,11 +86,11 @@ def test_pertensor_gemm_random_shapes(case):
                         oracle.tolerance_pertensor(A, B, sa, sb, r), what)
 
 
-@pytest.mark.parametrize("case", range(30))
+@pytest.mark.parametrize("case", range(30 * _MULT))
 def test_blockscaled_gemm_random_shapes(case):
     import torch
     fl = lib()
-    M, N, K = _shapes(202, 30)[case]
+    M, N, K = _shapes(202, 30 * _MULT)[case]
     rng = np.random.default_rng(2000 + case)
     A, B = random_codes(rng, (M, K)), random_codes(rng, (N, K))
     nkb = -(-K // 32)
@@ -110,7 +116,7 @@ def test_blockscaled_gemm_random_shapes(case):
                         oracle.tolerance_blockscaled_32x32(A, B, sa, sb, r), what)
 
 
-@pytest.mark.parametrize("case", range(24))
+@pytest.mark.parametrize("case", range(24 * _MULT))
 def test_grouped_gemm_random_shapes(case):
     import torch
     fl = lib()
@@ -161,7 +167,7 @@ def test_grouped_gemm_random_shapes(case):
                                 what + " group %d" % e)
 
 
-@pytest.mark.parametrize("case", range(30))
+@pytest.mark.parametrize("case", range(30 * _MULT))
 def test_quantisers_random_shapes(case):
     """Per-tensor (E4M3 and E5M2) and 32x32 block quantisation of random
     ragged shapes with padded row strides, bit for bit."""
@@ -190,7 +196,7 @@ def test_quantisers_random_shapes(case):
     assert np.array_equal(sb.cpu().numpy(), rsb), (rows, cols, pad)
 
 
-@pytest.mark.parametrize("case", range(16))
+@pytest.mark.parametrize("case", range(16 * _MULT))
 def test_grouped_quantiser_random_shapes(case):
     """Grouped per-tensor quantisation of random ragged groups (some empty)
     with padded strides and guard rows past the last group, bit for bit."""

@@ -186,3 +186,31 @@ def test_long_k_all_outputs(M, N, K, positive, variant):
     got = _gemm(fl, A, B, sa, sb)
     frac = check_pertensor(got, A, B, sa, sb, what="K %d" % K)
     assert frac > 0.9
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 300, 682), (340, 1, 682), (1, 1, 37), (1, 1, 4096)])
+def test_single_row_operands_unpadded(M, N, K):
+    """A or B with one row, K not a multiple of 16, passed as a contiguous
+    (unpadded) tensor through the torch-level call: a single row's stride
+    never addresses memory, so the binding passes a valid TMA stride for it.
+    A multi-row operand keeps a row stride padded to 16 bytes.  Every output
+    matches the oracle within the bound."""
+    import torch
+    fl = lib()
+    rng = np.random.default_rng(M * 7 + N * 3 + K)
+    A, B = random_codes(rng, (M, K)), random_codes(rng, (N, K))
+    sa, sb = np.float32(0.37), np.float32(1.9)
+
+    def dev(x):
+        if x.shape[0] == 1:
+            return to_dev(x)                      # [1][K], stride K
+        kp = (K + 15) // 16 * 16
+        d = torch.zeros((x.shape[0], kp), dtype=torch.uint8, device="cuda")
+        d[:, :K] = to_dev(x)
+        return d[:, :K]
+
+    C = fl.gemm(dev(A), dev(B), torch.tensor([sa], device="cuda"),
+                torch.tensor([sb], device="cuda"))
+    torch.cuda.synchronize()
+    assert fl.device_status() == 0
+    check_pertensor(bf16_to_f64(C), A, B, sa, sb, what="%dx%dx%d" % (M, N, K))
