@@ -222,3 +222,91 @@ def test_grouped_quantiser_random_shapes(case):
     assert np.array_equal(got[:rows, :cols], rq), (E, rows, cols, pad)
     assert np.array_equal(amax.cpu().numpy(), ramax) and np.array_equal(scale.cpu().numpy(), rscale)
     assert np.all(got[rows:] == 0xA5) and np.all(got[:, cols:] == 0xA5)
+
+
+@pytest.mark.parametrize("case", range(20 * _MULT))
+def test_quantisers_special_values_random(case):
+    """Per-tensor (E4M3, E5M2), delayed and block quantisers on random
+    ragged shapes with magnitudes spread over 40 binades and special values
+    (+-Inf, NaN, +-0, fp32 subnormals, the fp32 maximum) sprinkled in, bit
+    for bit."""
+    import torch
+    fl = lib()
+    rng = np.random.default_rng(6000 + case)
+    rows, cols = (int(v) for v in rng.integers(1, 400, 2))
+    x = (rng.standard_normal((rows, cols))
+         * 2.0 ** rng.uniform(-20, 20, (rows, cols))).astype(np.float32)
+    specials = np.array([np.inf, -np.inf, np.nan, 0.0, -0.0, 1e-41, -3e-39,
+                         3.4e38, -3.4e38], np.float32)
+    n_sp = int(rng.integers(0, 6))
+    if n_sp:
+        idx = rng.integers(0, x.size, n_sp)
+        x.reshape(-1)[idx] = rng.choice(specials, n_sp)
+    dx = to_dev(x)
+    fmt = ("e4m3", "e5m2")[case % 2]
+    q, amax, scale = fl.quantize_pertensor(dx, fmt=fmt)
+    torch.cuda.synchronize()
+    assert fl.device_status() == 0
+    rq, ramax, rscale = oracle.quantize_pertensor(x, fmt=fmt)
+    assert np.array_equal(q.cpu().numpy(), rq), (rows, cols, fmt)
+    assert np.float32(amax.item()).tobytes() == np.float32(ramax).tobytes()
+    assert np.float32(scale.item()).tobytes() == np.float32(rscale).tobytes()
+    prev = float(rng.choice([ramax, 1.0, 1e-30, np.inf, 448.0]))
+    dprev = torch.tensor([prev], dtype=torch.float32, device="cuda")
+    q2, amax2, scale2 = fl.quantize_pertensor_delayed(dx, dprev, fmt=fmt)
+    torch.cuda.synchronize()
+    assert fl.device_status() == 0
+    rq2, ramax2, rscale2 = oracle.quantize_pertensor_delayed(x, prev, fmt)
+    assert np.array_equal(q2.cpu().numpy(), rq2), (rows, cols, fmt, prev)
+    assert np.float32(amax2.item()).tobytes() == np.float32(ramax2).tobytes()
+    assert np.float32(scale2.item()).tobytes() == np.float32(rscale2).tobytes()
+    qb, sbk = fl.quantize_blockwise_32x32(dx)
+    torch.cuda.synchronize()
+    assert fl.device_status() == 0
+    rqb, rsb = oracle.quantize_blockwise_32x32(x)
+    assert np.array_equal(qb.cpu().numpy(), rqb), (rows, cols)
+    assert np.array_equal(sbk.cpu().numpy().view(np.uint32), rsb.view(np.uint32))
+
+
+@pytest.mark.parametrize("case", range(20 * _MULT))
+def test_gemms_wide_scale_ranges(case):
+    """Per-tensor GEMM with scale pairs whose product spans 1e-25 .. 1e25 and
+    block-scaled GEMM with tile scales spread over 1e-6 .. 1e6, random ragged
+    shapes; every output within the bound."""
+    import torch
+    fl = lib()
+    rng = np.random.default_rng(7000 + case)
+    M, N, K = (int(v) for v in rng.integers(1, 500, 3))
+    A, B = random_codes(rng, (M, K)), random_codes(rng, (N, K))
+    e = rng.uniform(-25, 25)
+    f = rng.uniform(0, 1)
+    sa, sb = np.float32(10.0 ** (e * f)), np.float32(10.0 ** (e * (1 - f)))
+    variant = [0, 1, 2, 3, 4][case % 5]
+    fl.fp8la_set_gemm_variant(variant)
+    try:
+        C = fl.gemm(_dev_codes(A), _dev_codes(B), torch.tensor([sa], device="cuda"),
+                    torch.tensor([sb], device="cuda"))
+        torch.cuda.synchronize()
+    finally:
+        fl.fp8la_set_gemm_variant(0)
+    assert fl.device_status() == 0
+    what = "%dx%dx%d sa %g sb %g variant %d" % (M, N, K, sa, sb, variant)
+    r, _ = oracle.gemm_pertensor(A, B, sa, sb)
+    assert_within_bound(bf16_to_f64(C), r, oracle.tolerance_pertensor(A, B, sa, sb, r), what)
+    nkb = -(-K // 32)
+    ta = (10.0 ** rng.uniform(-6, 6, (-(-M // 32), nkb))).astype(np.float32)
+    tb = (10.0 ** rng.uniform(-6, 6, (-(-N // 32), nkb))).astype(np.float32)
+
+    def dev_scales(s):
+        d = torch.zeros((s.shape[0], (s.shape[1] + 3) // 4 * 4), dtype=torch.float32,
+                        device="cuda")
+        d[:, :s.shape[1]] = to_dev(s)
+        return d[:, :s.shape[1]]
+
+    C2 = fl.gemm_blockscaled_32x32(_dev_codes(A), _dev_codes(B), dev_scales(ta), dev_scales(tb))
+    torch.cuda.synchronize()
+    assert fl.device_status() == 0
+    r2, _ = oracle.gemm_blockscaled_32x32(A, B, ta, tb)
+    assert_within_bound(bf16_to_f64(C2), r2,
+                        oracle.tolerance_blockscaled_32x32(A, B, ta, tb, r2),
+                        "block-scaled %dx%dx%d" % (M, N, K))
