@@ -621,7 +621,9 @@ def _workload_pertensor(fl, torch, dev, sptr, ph, delayed=False):
     # while still in use.
     e2e = {}
 
-    def ebegin(A_h, B_h, C_h2):
+    def ebegin(host_inputs, host_outputs2):
+        A_h, B_h = host_inputs
+        C_h2 = host_outputs2[0]
         if not e2e:
             e2e.update(A=[A, torch.empty_like(A)], B=[B, torch.empty_like(B)],
                        C=[C, torch.empty_like(C)],
@@ -831,21 +833,80 @@ def _workload_blockscaled(fl, torch, dev, sptr, ph, linears=("qkv", "attn_out", 
         qelems += M * K + N * K
         gbytes += M * K + N * K + 2 * M * N + 4 * (sx.numel() + sw.numel())
 
-    def step():
-        for (M, N, K, X, W, qx, qw, sx, sw, C, _, _) in items:
-            ph.mark("quant")
+    def run(xs, ws, cs, s, mark=True):
+        for (M, N, K, _, _, qx, qw, sx, sw, _, _, _), X, W, C in zip(items, xs, ws, cs):
+            if mark:
+                ph.mark("quant")
             fl.fp8_quantize_blockwise_32x32(X.data_ptr(), M, K, K, qx.data_ptr(), K,
-                                            sx.data_ptr(), sx.stride(0), sptr)
+                                            sx.data_ptr(), sx.stride(0), s)
             fl.fp8_quantize_blockwise_32x32(W.data_ptr(), N, K, K, qw.data_ptr(), K,
-                                            sw.data_ptr(), sw.stride(0), sptr)
-            ph.mark("quant")
-            ph.mark("gemm")
+                                            sw.data_ptr(), sw.stride(0), s)
+            if mark:
+                ph.mark("quant")
+                ph.mark("gemm")
             fl.fp8_gemm_blockscaled_32x32(qx.data_ptr(), K, qw.data_ptr(), K, C.data_ptr(), N,
                                           M, N, K, sx.data_ptr(), sx.stride(0),
-                                          sw.data_ptr(), sw.stride(0), sptr)
-            ph.mark("gemm")
+                                          sw.data_ptr(), sw.stride(0), s)
+            if mark:
+                ph.mark("gemm")
 
-    return dict(step=step, flops=flops, launches=12, quant_bytes_per_elem=5, gemm_bound="alu",
+    def step():
+        run([it[3] for it in items], [it[4] for it in items], [it[9] for it in items], sptr)
+
+    # Pipelined end to end, as for the 8192^3 workload: step i's fp32
+    # activations and weights come from pinned host memory on a copy stream,
+    # its outputs go back on another; the host->device copies of step i+1,
+    # the compute of step i (one stream, so codes and scales need no second
+    # copy) and the device->host copies of step i-1 overlap.  Device inputs
+    # and outputs are double-buffered.
+    main = torch.cuda.current_stream(dev)
+    nl = len(items)
+    e2e = {}
+
+    def ebegin(host_inputs, host_outputs2):
+        if not e2e:
+            e2e.update(
+                X=[[it[3] for it in items], [torch.empty_like(it[3]) for it in items]],
+                W=[[it[4] for it in items], [torch.empty_like(it[4]) for it in items]],
+                C=[[it[9] for it in items], [torch.empty_like(it[9]) for it in items]],
+                si=torch.cuda.Stream(dev), sc=torch.cuda.Stream(dev),
+                so=torch.cuda.Stream(dev),
+                computed=[torch.cuda.Event(), torch.cuda.Event()],
+                stored=[torch.cuda.Event(), torch.cuda.Event()])
+        e2e.update(X_h=host_inputs[:nl], W_h=host_inputs[nl:], C_h=host_outputs2)
+        for k in ("computed", "stored"):
+            for ev in e2e[k]:
+                ev.record(main)
+        for st in (e2e["si"], e2e["sc"], e2e["so"]):
+            st.wait_stream(main)
+
+    def estep(i):
+        b = i & 1
+        T = e2e
+        # inputs: buffer b is free once the compute of step i-2 has read it
+        T["si"].wait_event(T["computed"][b])
+        with torch.cuda.stream(T["si"]):
+            for d, h in zip(T["X"][b] + T["W"][b], T["X_h"] + T["W_h"]):
+                d.copy_(h, non_blocking=True)
+        loaded = torch.cuda.Event()
+        loaded.record(T["si"])
+        # compute into C[b] once the device->host copies of step i-2 have read it
+        T["sc"].wait_event(loaded)
+        T["sc"].wait_event(T["stored"][b])
+        run(T["X"][b], T["W"][b], T["C"][b], T["sc"].cuda_stream, mark=False)
+        T["computed"][b].record(T["sc"])
+        T["so"].wait_event(T["computed"][b])
+        with torch.cuda.stream(T["so"]):
+            for k in range(nl):
+                T["C_h"][k][b].copy_(T["C"][b][k], non_blocking=True)
+        T["stored"][b].record(T["so"])
+
+    def eend():
+        for st in (e2e["si"], e2e["sc"], e2e["so"]):
+            main.wait_stream(st)
+
+    return dict(step=step, e2e_pipeline=(ebegin, estep, eend),
+                flops=flops, launches=12, quant_bytes_per_elem=5, gemm_bound="alu",
                 per_op=[(name, 2.0 * it[0] * it[1] * it[2]) for name, it in zip(linears, items)],
                 workload=("32x32 block-scaled E4M3: block-quantize activations [4096][K] ~ N(0,1) "
                           "and weights [N][K] ~ N(0,0.02), then the block-scaled GEMM, for the "
@@ -958,7 +1019,9 @@ def _workload_grouped(fl, torch, dev, sptr, ph):
     # both directions at once).  Device inputs and C are double-buffered.
     e2e = {}
 
-    def ebegin(X_h, W_h, C_h2):
+    def ebegin(host_inputs, host_outputs2):
+        X_h, W_h = host_inputs
+        C_h2 = host_outputs2[0]
         if not e2e:
             e2e.update(X=[X, torch.empty_like(X)], W=[W, torch.empty_like(W)],
                        C=[C, torch.empty_like(C)],
@@ -1259,16 +1322,17 @@ def run_gpu(args):
     torch.cuda.synchronize()
     if e2e_pipelined:
         ebegin, estep, eend = W["e2e_pipeline"]
-        C_h2 = [outs[0][1], torch.empty_like(outs[0][1]).pin_memory()]
+        outs2 = [[h, torch.empty_like(h).pin_memory()] for _, h in outs]
+        host_inputs = [h for _, h in hosts]
         e2e_serial_runs = [time_serial() for _ in range(E2E_REPEATS)]
-        ebegin(hosts[0][1], hosts[1][1], C_h2)
+        ebegin(host_inputs, outs2)
         for i in range(3):
             estep(i)
         eend()
         torch.cuda.synchronize()
         for _ in range(E2E_REPEATS):
             e0.record(stream)
-            ebegin(hosts[0][1], hosts[1][1], C_h2)
+            ebegin(host_inputs, outs2)
             for i in range(e2e_steps):
                 estep(i)
             eend()
@@ -1279,14 +1343,17 @@ def run_gpu(args):
         e2e_runs = [time_serial() for _ in range(E2E_REPEATS)]
     e2e_equal = None
     if e2e_pipelined:
-        # The host copy of the last pipelined step's output against the
-        # device output of a plain step on the same inputs, bit for bit.
-        last = C_h2[(e2e_steps - 1) & 1]
+        # The host copies of the last pipelined step's outputs against the
+        # device outputs of a plain step on the same inputs, bit for bit.
         step()
         torch.cuda.synchronize()
-        dev_out = outs[0][0].cpu()
-        e2e_equal = bool(torch.equal(last.view(torch.int16), dev_out.view(torch.int16)))
-        del dev_out
+        e2e_equal = True
+        for k, (o, _) in enumerate(outs):
+            last = outs2[k][(e2e_steps - 1) & 1]
+            dev_out = o.cpu()
+            e2e_equal = e2e_equal and bool(torch.equal(last.view(torch.int16),
+                                                       dev_out.view(torch.int16)))
+            del dev_out
     e2e_ms = statistics.median(e2e_runs)
     e2e_serial_ms = statistics.median(e2e_serial_runs) if e2e_serial_runs else None
     if world > 1:
