@@ -1126,20 +1126,70 @@ def _workload_attention(fl, torch, dev, sptr, ph, batch=2, heads=64, seq=2048, h
     S = torch.empty((E * seq, seq), dtype=torch.bfloat16, device=dev)
     O = torch.empty((E * seq, hd), dtype=torch.bfloat16, device=dev)
 
+    def run(q4, so, s):
+        q_Q, q_K, q_P, q_V = q4
+        S_, O_ = so
+        fl.fp8_grouped_gemm(E, offs.data_ptr(), E * seq, Pp(q_Q), hd, Pp(q_K), hd, seq * hd,
+                            Pp(S_), seq, seq, hd, Pp(sc, 0), Pp(sc, E), s)
+        fl.fp8_grouped_gemm(E, offs.data_ptr(), E * seq, Pp(q_P), seq, Pp(q_V), seq, hd * seq,
+                            Pp(O_), hd, hd, seq, Pp(sc, 2 * E), Pp(sc, 3 * E), s)
+
     def step():
         ph.mark("quant")
         ph.mark("quant")
         ph.mark("gemm")
-        fl.fp8_grouped_gemm(E, offs.data_ptr(), E * seq, Pp(qQ), hd, Pp(qK), hd, seq * hd,
-                            Pp(S), seq, seq, hd, Pp(sc, 0), Pp(sc, E), sptr)
-        fl.fp8_grouped_gemm(E, offs.data_ptr(), E * seq, Pp(qP), seq, Pp(qV), seq, hd * seq,
-                            Pp(O), hd, hd, seq, Pp(sc, 2 * E), Pp(sc, 3 * E), sptr)
+        run((qQ, qK, qP, qV), (S, O), sptr)
         ph.mark("gemm")
+
+    # Pipelined end to end: step i+1's codes go to the device on one copy
+    # stream while step i's two GEMMs run and step i-1's scores and outputs
+    # come back on another; device codes, S and O are double-buffered.
+    main = torch.cuda.current_stream(dev)
+    e2e = {}
+
+    def ebegin(host_inputs, host_outputs2):
+        if not e2e:
+            e2e.update(Q=[[qQ, qK, qP, qV], [torch.empty_like(t) for t in (qQ, qK, qP, qV)]],
+                       R=[[S, O], [torch.empty_like(S), torch.empty_like(O)]],
+                       si=torch.cuda.Stream(dev), sc=torch.cuda.Stream(dev),
+                       so=torch.cuda.Stream(dev),
+                       computed=[torch.cuda.Event(), torch.cuda.Event()],
+                       stored=[torch.cuda.Event(), torch.cuda.Event()])
+        e2e.update(H=host_inputs, R_h=host_outputs2)
+        for k in ("computed", "stored"):
+            for ev in e2e[k]:
+                ev.record(main)
+        for st in (e2e["si"], e2e["sc"], e2e["so"]):
+            st.wait_stream(main)
+
+    def estep(i):
+        b = i & 1
+        T = e2e
+        T["si"].wait_event(T["computed"][b])
+        with torch.cuda.stream(T["si"]):
+            for d, h in zip(T["Q"][b], T["H"]):
+                d.copy_(h, non_blocking=True)
+        loaded = torch.cuda.Event()
+        loaded.record(T["si"])
+        T["sc"].wait_event(loaded)
+        T["sc"].wait_event(T["stored"][b])
+        run(T["Q"][b], T["R"][b], T["sc"].cuda_stream)
+        T["computed"][b].record(T["sc"])
+        T["so"].wait_event(T["computed"][b])
+        with torch.cuda.stream(T["so"]):
+            for k in range(2):
+                T["R_h"][k][b].copy_(T["R"][b][k], non_blocking=True)
+        T["stored"][b].record(T["so"])
+
+    def eend():
+        for st in (e2e["si"], e2e["sc"], e2e["so"]):
+            main.wait_stream(st)
 
     flops = 2.0 * 2 * E * seq * seq * hd
     codes = [(qQ, qQ.cpu().numpy()), (qK, qK.cpu().numpy()), (qP, qP.cpu().numpy()),
              (qV, qV.cpu().numpy())]
-    return dict(step=step, flops=flops, launches=2, gemm_bound="hbm",
+    return dict(step=step, e2e_pipeline=(ebegin, estep, eend),
+                flops=flops, launches=2, gemm_bound="hbm",
                 workload=("FP8 attention GEMMs (scores = Q K^T, out = P V), non-causal, batch %d x "
                           "%d heads, seq %d, head_dim %d, E4M3 inputs with per-head scales "
                           "(quantised at set-up); two grouped launches per step; seed 0"
