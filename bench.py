@@ -770,6 +770,22 @@ def _workload_square(n):
             quant(stream_ptr)
             gemm(stream_ptr)
 
+        def launches_forked(main_s, side_s):
+            # The two quantisations are independent: B's runs on a side
+            # stream forked from and joined back into the main one, so the
+            # captured graph holds them as parallel branches.
+            fork = torch.cuda.Event()
+            fork.record(main_s)
+            side_s.wait_event(fork)
+            fl.fp8_quantize_pertensor_ex(P(A), n, n, n, P(qa), n, P(amax, 0), P(scale, 0),
+                                         f, main_s.cuda_stream)
+            fl.fp8_quantize_pertensor_ex(P(B), n, n, n, P(qb), n, P(amax, 1), P(scale, 1),
+                                         f, side_s.cuda_stream)
+            join = torch.cuda.Event()
+            join.record(side_s)
+            main_s.wait_event(join)
+            gemm(main_s.cuda_stream)
+
         def step():
             ph.mark("quant")
             quant(sptr)
@@ -786,16 +802,18 @@ def _workload_square(n):
             launches(cap.cuda_stream)
         torch.cuda.current_stream(dev).wait_stream(cap)
         torch.cuda.synchronize()
+        side = torch.cuda.Stream(dev)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=cap):
-            launches(cap.cuda_stream)
+            launches_forked(cap, side)
         torch.cuda.synchronize()
         # Kernels per step: tensors of at most 512K floats take the one-launch
         # quantiser, larger ones amax + cast.
         per_operand = 1 if n * n <= (1 << 19) else 2
         return dict(step=step, graph=graph, flops=2.0 * n ** 3, launches=2 * per_operand + 1,
                     workload=("per-tensor %s quantize(A), quantize(B) + scaled GEMM, "
-                              "M=N=K=%d, A, B ~ N(0,1), seed 0; one CUDA graph per step"
+                              "M=N=K=%d, A, B ~ N(0,1), seed 0; one CUDA graph per step, the two "
+                              "quantisations as parallel branches"
                               % (_SQUARE_OPTS["fmt"].upper(), n)),
                     config={"M": n, "N": n, "K": n, "format": _SQUARE_OPTS["fmt"],
                             "gemm_variant": _SQUARE_OPTS["gemm_variant"],
