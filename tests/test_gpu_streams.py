@@ -202,3 +202,82 @@ def test_cuda_graph_capture_and_replay():
     torch.cuda.synchronize()
     assert torch.equal(qa, ref_qa) and torch.equal(qb, ref_qb)
     assert fl.device_status() == 0
+
+
+def test_blockscaled_linears_pipeline_matches_serial():
+    """Several linears in a row, pipelined per linear: linear k+1's block
+    quantisation (activations and weights) on one stream while linear k's
+    block-scaled GEMM runs on another, across step boundaries, each linear
+    with its own code and scale buffers.  Same results as the serial steps,
+    bit for bit; every step has new activations."""
+    import torch
+    fl = lib()
+    rng = np.random.default_rng(41)
+    shapes = [(96, 160, 256), (96, 64, 320), (96, 224, 96)]      # (M, N, K) per linear
+    steps = 4
+    Ws = [to_dev((rng.standard_normal((N, K)) * 0.02).astype(np.float32)) for _, N, K in shapes]
+    Xs = [[to_dev(rng.standard_normal((M, K)).astype(np.float32)) for M, _, K in shapes]
+          for _ in range(steps)]
+
+    def buffers(M, N, K):
+        kb = (K + 31) // 32
+        sc = lambda r: torch.zeros((r, (kb + 3) // 4 * 4), dtype=torch.float32,
+                                   device="cuda")[:, :kb]
+        return (torch.empty((M, K), dtype=torch.uint8, device="cuda"),
+                torch.empty((N, K), dtype=torch.uint8, device="cuda"),
+                sc((M + 31) // 32), sc((N + 31) // 32))
+
+    def quant(k, x, buf, s):
+        M, N, K = shapes[k]
+        qx, qw, sx, sw = buf
+        fl.fp8_quantize_blockwise_32x32(x.data_ptr(), M, K, K, qx.data_ptr(), K,
+                                        sx.data_ptr(), sx.stride(0), s)
+        fl.fp8_quantize_blockwise_32x32(Ws[k].data_ptr(), N, K, K, qw.data_ptr(), K,
+                                        sw.data_ptr(), sw.stride(0), s)
+
+    def gemm(k, buf, out, s):
+        M, N, K = shapes[k]
+        qx, qw, sx, sw = buf
+        fl.fp8_gemm_blockscaled_32x32(qx.data_ptr(), K, qw.data_ptr(), K, out.data_ptr(), N,
+                                      M, N, K, sx.data_ptr(), sx.stride(0), sw.data_ptr(),
+                                      sw.stride(0), s)
+
+    def outputs():
+        return [[torch.full((M, N), 9.0, dtype=torch.bfloat16, device="cuda")
+                 for M, N, _ in shapes] for _ in range(steps)]
+
+    cur = torch.cuda.current_stream().cuda_stream
+    bufs = [buffers(*sh) for sh in shapes]
+    ref = outputs()
+    for i in range(steps):
+        for k in range(len(shapes)):
+            quant(k, Xs[i][k], bufs[k], cur)
+            gemm(k, bufs[k], ref[i][k], cur)
+    torch.cuda.synchronize()
+
+    bufs = [buffers(*sh) for sh in shapes]
+    got = outputs()
+    main = torch.cuda.current_stream()
+    sq, sg = torch.cuda.Stream(), torch.cuda.Stream()
+    qdone = [torch.cuda.Event() for _ in shapes]
+    gdone = [torch.cuda.Event() for _ in shapes]
+    for ev in qdone + gdone:
+        ev.record(main)
+    sq.wait_stream(main)
+    sg.wait_stream(main)
+    for i in range(steps):
+        for k in range(len(shapes)):
+            sq.wait_event(gdone[k])
+            quant(k, Xs[i][k], bufs[k], sq.cuda_stream)
+            qdone[k].record(sq)
+            sg.wait_event(qdone[k])
+            gemm(k, bufs[k], got[i][k], sg.cuda_stream)
+            gdone[k].record(sg)
+    main.wait_stream(sq)
+    main.wait_stream(sg)
+    torch.cuda.synchronize()
+    assert fl.device_status() == 0
+    for i in range(steps):
+        for k in range(len(shapes)):
+            assert torch.equal(got[i][k].view(torch.int16), ref[i][k].view(torch.int16)), (i, k)
+    assert not torch.equal(ref[0][0], ref[1][0])
