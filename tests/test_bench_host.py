@@ -73,14 +73,17 @@ def test_nvsmi_timestamps_parse():
 
 def test_peak_regime():
     capped = _c(["sw_power_cap"], sm=1777.0)
-    assert bench._peak_regime(420.0, capped, True, False)[0]
+    # only a timed region of seconds is rated against the sustained figure
     assert bench._peak_regime(2500.0, _c([]), True, False)[0]
-    # short, unthrottled regions, graph replays and a missing sustained
-    # figure are rated against the burst figure
+    assert bench._peak_regime(2500.0, capped, True, False)[0]
+    # shorter regions (power-capped or not), graph replays and a missing
+    # sustained figure are rated against the burst figure
+    assert not bench._peak_regime(420.0, capped, True, False)[0]
+    assert "sw_power_cap" in bench._peak_regime(420.0, capped, True, False)[1]
     assert not bench._peak_regime(8.0, _c([]), True, False)[0]
     assert not bench._peak_regime(8.0, _c(["sw_power_cap"], sm=2060.0), True, False)[0]
-    assert not bench._peak_regime(420.0, capped, True, True)[0]
-    assert not bench._peak_regime(420.0, capped, False, False)[0]
+    assert not bench._peak_regime(2500.0, capped, True, True)[0]
+    assert not bench._peak_regime(2500.0, capped, False, False)[0]
 
 
 def test_alu_promotion_peak():
